@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark of the exact attention forward library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one call of the hot path over one batch of synthetic input:
+attn_fwd for the prefill / training workloads (one kernel launch), or
+attn_fwd_splitkv for the decode workload (split kernel + combine kernel).
+Default workload: the training shape B=4, H=16, N=4096, d=128, causal.
+
+value: device-resident throughput (inputs already in HBM), CUDA events around
+each step on the launching stream, L2 flushed (256 MB write) before every
+timed step, summed over K steps, max over ranks; whole-job aggregate.
+e2e: the same metric through the same C-ABI call with host buffers: every
+step copies the inputs from pinned host memory and the outputs back.
+For N > 1 (torchrun) every rank runs an independent replica of the workload
+(weak scaling; the path has no exchange step).
+
+--impl reference times the fp64 CPU oracle (the correctness reference) on
+the host cores, each step a bounded sample of the same workload, and prints
+the same line with "impl": "reference".
+"""
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s and % of GB300 BF16 peak; decode GB/s and % of HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- clocks (NVML via ctypes)
+class ClockSampler:
+    """Samples SM clock and clock-event reasons every few ms while running."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, torch_device_index):
+        self.ok = False
+        self.samples = []
+        self.reason_bits = 0
+        self.max_mhz = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.nv = nv
+            self.h = ctypes.c_void_p()
+            import torch
+            bus = None
+            try:
+                props = torch.cuda.get_device_properties(torch_device_index)
+                bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            except Exception:
+                bus = None
+            rc = 1
+            if bus is not None:
+                rc = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(0), ctypes.byref(self.h))
+            if rc != 0:
+                return
+            m = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self.get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _run(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if self.get_reasons(self.h, ctypes.byref(r)) == 0:
+                self.reason_bits |= r.value
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "source": "unavailable"}
+        reasons = [n for bit, n in sorted(self.REASONS.items()) if self.reason_bits & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "nvml"}
+
+
+# --------------------------------------------------------------------------- workloads
+def get_workload(name):
+    from exact_io_aware_14_gb300 import workloads as W
+    table = {"tiny": W.TINY, "train_causal": W.TRAIN_CAUSAL, "train": W.TRAIN, "gqa": W.GQA, "long": W.LONG,
+             "decode": W.DECODE}
+    return table[name]
+
+
+def config_of(w, n_gpus):
+    from exact_io_aware_14_gb300 import workloads as W
+    if isinstance(w, W.Decode):
+        cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "max_seqlen": w.max_seqlen, "d": w.d,
+               "chunk": w.chunk, "seqlens": "U[%d,%d] int32, seed %d" % (w.len_lo, w.len_hi, w.seed)}
+    else:
+        cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.N, "Nk": w.N, "d": w.d,
+               "causal": w.causal, "scale": "1/sqrt(d)"}
+    cfg["l2"] = "flushed before every timed step (256 MB write)"
+    cfg["parallelism"] = "replicas x%d (independent, no exchange)" % n_gpus if n_gpus > 1 else "single GPU"
+    return cfg
+
+
+def decode_bytes(w, seqlens):
+    kv = sum(2 * int(L) * w.Hkv * w.d * 2 for L in seqlens)
+    return kv + 2 * (w.B * w.Hq * w.d * 2) + w.B * w.Hq * 4
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(w, q, k, v, seqlens, budget_s, seed):
+    """Times the fp64 oracle on a seeded sample of rows sized to ~budget_s.
+    Returns (value in the metric's unit, seconds, description, threads)."""
+    import numpy as np
+    import oracle
+    from exact_io_aware_14_gb300 import workloads as W
+    threads = oracle.host_threads()
+    dec = isinstance(w, W.Decode)
+    Nq = 1 if dec else w.N
+
+    def rows_and_work(n):
+        rows = W.sample_rows(w.B, w.Hq, Nq, n, seed=seed)
+        if dec:
+            work = sum(2 * int(seqlens[b]) * w.d * 2 for b, _, _ in rows)   # bytes of K and V rows read
+        else:
+            work = sum(4.0 * ((i + 1) if w.causal else w.N) * w.d for _, _, i in rows)  # FLOPs
+        return rows, work
+
+    def run(n):
+        rows, work = rows_and_work(n)
+        t0 = time.perf_counter()
+        oracle.attn_rows(q, k, v, rows, False if dec else w.causal, w.scale,
+                         kv_len=(seqlens if dec else None), n_threads=threads)
+        return work, time.perf_counter() - t0, len(rows)
+
+    n = max(threads, 16)
+    work, dt, _ = run(n)
+    while dt < 0.2 and n < (w.B * w.Hq * Nq):
+        n *= 4
+        work, dt, _ = run(n)
+    n_target = int(min(w.B * w.Hq * Nq, max(n, n * budget_s / max(dt, 1e-6))))
+    work, dt, nrows = run(n_target)
+    if dec:
+        value = work / dt / 1e9
+        desc = "%d seeded (b, hq) rows of the decode workload, all valid keys each (%.1f s)" % (nrows, dt)
+    else:
+        value = work / dt / 1e12
+        desc = "%d seeded query rows of the workload, every visible key (%.1f s)" % (nrows, dt)
+    return value, dt, desc, threads
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    from exact_io_aware_14_gb300 import _native, build as native_build, workloads as W
+
+    if rank == 0:
+        native_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+        native_build.build()  # no-op once rank 0 has built it
+    _native.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device=dev).manual_seed(1234 + w.seed + rank)
+    dec = isinstance(w, W.Decode)
+
+    def randn(shape, amp=1.0):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+        if amp != 1.0:
+            x.mul_(amp)
+        return x.to(torch.bfloat16)
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if dec:
+        q = randn((w.B, 1, w.Hq, w.d))
+        k = randn((w.B, w.max_seqlen, w.Hkv, w.d))
+        v = randn((w.B, w.max_seqlen, w.Hkv, w.d))
+        seqlens = torch.randint(w.len_lo, w.len_hi + 1, (w.B,), generator=gen, device=dev, dtype=torch.int32)
+        pos = torch.arange(w.max_seqlen, device=dev)[None, :, None, None]
+        bad = pos >= seqlens.long()[:, None, None, None]
+        k.masked_fill_(bad, float("nan"))
+        v.masked_fill_(bad, float("nan"))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
+        ws = torch.empty(_native.attn_splitkv_workspace_size(w.B, w.Hq, w.max_seqlen, w.d, w.chunk),
+                         dtype=torch.uint8, device=dev)
+        L_host = seqlens.cpu().tolist()
+        work = decode_bytes(w, L_host)
+        unit, scale_unit = "GB/s", 1e9
+        launches_per_step = 2
+
+        def step():
+            rc = _native.attn_fwd_splitkv(q, k, v, seqlens, o, lse, w.scale, w.chunk, ws, stream)
+            if rc != 0:
+                raise RuntimeError("attn_fwd_splitkv: %s" % _native.status_string(rc))
+    else:
+        q = randn((w.B, w.N, w.Hq, w.d), w.amp)
+        k = randn((w.B, w.N, w.Hkv, w.d), w.amp)
+        v = randn((w.B, w.N, w.Hkv, w.d), w.amp)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+        work = w.flops()
+        unit, scale_unit = "TFLOP/s", 1e12
+        launches_per_step = 1
+
+        def step():
+            rc = _native.attn_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+            if rc != 0:
+                raise RuntimeError("attn_fwd: %s" % _native.status_string(rc))
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if _native.attn_get_device_status(stream) != 0:
+        raise RuntimeError("device status error after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with sampler:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    wall1 = time.perf_counter()
+    if world > 1:
+        torch.distributed.barrier()
+    if _native.attn_get_device_status(stream) != 0:
+        raise RuntimeError("device status error in the timed region")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = t.item()
+    ms_per_step = total_ms / args.steps
+    value = world * work / (ms_per_step * 1e-3) / scale_unit
+    kernel_rate = work / (statistics.mean(step_ms) * 1e-3) / scale_unit
+
+    # ---- e2e through host buffers (pinned), copies inside the timed region
+    if dec:
+        h_in = [x.cpu().pin_memory() for x in (q, k, v, seqlens)]
+        d_in = [q, k, v, seqlens]
+        h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (o, lse)]
+    else:
+        h_in = [x.cpu().pin_memory() for x in (q, k, v)]
+        d_in = [q, k, v]
+        h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (o, lse)]
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for d_t, h_t in zip(d_in, h_in):
+            d_t.copy_(h_t, non_blocking=True)
+        step()
+        h_out[0].copy_(o, non_blocking=True)
+        h_out[1].copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        es[i].record(stream)
+        e2e_step()
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = t.item()
+    e2e_value = world * work / (e2e_ms * 1e-3) / scale_unit
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    if dec:
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": kernel_rate, "peak": peak, "unit": "GB/s",
+                "frac": kernel_rate / peak, "traffic": None,
+                "peak_source": "%s hbm_gbs (copy)" % peak_src,
+                "kernel": "decode split + combine (one step, both launches)",
+                "algorithmic_bytes_per_step": work}
+    else:
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": kernel_rate, "peak": peak, "unit": "TFLOP/s",
+                "frac": kernel_rate / peak, "traffic": None,
+                "peak_source": "%s bf16_tflops (burst cuBLAS)" % peak_src,
+                "kernel": "prefill_fwd_kernel<%d>" % w.d, "algorithmic_flops_per_launch": work}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+        sl = seqlens.cpu().numpy() if dec else None
+        val, dt, desc, thr = oracle_sample_rate(w, qc, kc, vc, sl, args.cpu_seconds, seed=w.seed)
+        cpu = {"value": val, "unit": unit, "cores": thr, "kind": "oracle", "sample": desc}
+
+    return {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) fp32 draws rounded to bf16, generated on the device",
+        "config": config_of(w, world), "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": sampler.summary(),
+        "timed_wall_s": wall1 - wall0,
+    }
+
+
+# --------------------------------------------------------------------------- reference arm (CPU oracle)
+def run_reference(args, w):
+    import torch
+    from exact_io_aware_14_gb300 import workloads as W
+    dec = isinstance(w, W.Decode)
+    # a bounded slice of the same workload on the CPU (same seeds and recipe)
+    if dec:
+        q, k, v, L = W.workload_decode_inputs(w)
+        sl = L.numpy()
+        unit = "GB/s"
+    else:
+        q, k, v = W.workload_inputs(w)
+        sl = None
+        unit = "TFLOP/s"
+    per_step = max(0.2, min(8.0, args.reference_seconds / max(1, args.steps + args.warmup)))
+    vals, secs, desc, thr = [], [], "", 1
+    for i in range(args.warmup + args.steps):
+        val, dt, desc, thr = oracle_sample_rate(w, q, k, v, sl, per_step, seed=w.seed + 17 * i)
+        if i >= args.warmup:
+            vals.append(val)
+            secs.append(dt)
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) fp32 draws rounded to bf16 (CPU generator)",
+        "config": config_of(w, 1),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": thr, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="train_causal",
+                    choices=["tiny", "train_causal", "train", "gqa", "long", "decode"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
+    ap.add_argument("--reference-seconds", type=float, default=90.0, help="whole reference-arm budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = get_workload(args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,144 @@
+"""ctypes binding of libattn_sm103.so (include/attn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  If the library has not been built, the first call raises -- there
+is no fallback of any kind.
+"""
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libattn_sm103.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "attn.h")
+
+ATTN_OK = 0
+STATUS_NAMES = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
+    4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT", 6: "ATTN_ERR_DEVICE_ARG", 7: "ATTN_ERR_WORKSPACE",
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__("%s failed: %s (%s)" % (what, STATUS_NAMES.get(code, code), status_string(code)))
+
+
+def declared_functions():
+    """Names of the functions include/attn.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:ATTN_API\s+)?(?:const\s+)?\w+\**\s+\**(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("CUDA attention library not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        L.attn_fwd.restype = i
+        L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        L.attn_splitkv_workspace_size.restype = sz
+        L.attn_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+        L.attn_fwd_splitkv.restype = i
+        L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+        L.attn_get_device_status.restype = i
+        L.attn_get_device_status.argtypes = [vp]
+        L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_status_string.argtypes = [i]
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().attn_status_string(int(code)).decode()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check_bf16(name, t, shape):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must be a contiguous CUDA bf16 tensor of shape %s (got %s %s %s)"
+                         % (name, tuple(shape), t.dtype, tuple(t.shape), t.device))
+
+
+# --------------------------------------------------------------------------- raw entry points
+def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
+    """Same contract as the C call: writes o [B,Nq,Hq,d] and lse [B,Hq,Nq]. Returns the status."""
+    B, Nq, Hq, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    _check_bf16("q", q, (B, Nq, Hq, d))
+    _check_bf16("k", k, (B, Nk, Hkv, d))
+    _check_bf16("v", v, (B, Nk, Hkv, d))
+    _check_bf16("o", o, (B, Nq, Hq, d))
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor of shape %s" % ((B, Hq, Nq),))
+    return lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                          int(bool(causal)), float(scale), _stream_handle(stream))
+
+
+def attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk):
+    return int(lib().attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk))
+
+
+def attn_fwd_splitkv(q, k_cache, v_cache, seqlens, o, lse, scale, chunk, workspace, stream=None):
+    """Same contract as the C call. workspace: a CUDA uint8 tensor. Returns the status."""
+    B, _, Hq, d = q.shape
+    max_seqlen, Hkv = k_cache.shape[1], k_cache.shape[2]
+    _check_bf16("q", q, (B, 1, Hq, d))
+    _check_bf16("k_cache", k_cache, (B, max_seqlen, Hkv, d))
+    _check_bf16("v_cache", v_cache, (B, max_seqlen, Hkv, d))
+    _check_bf16("o", o, (B, 1, Hq, d))
+    if seqlens.dtype != torch.int32 or not seqlens.is_cuda or tuple(seqlens.shape) != (B,):
+        raise ValueError("seqlens must be a CUDA int32 tensor of shape (%d,)" % B)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, Hq, 1):
+        raise ValueError("lse must be a CUDA fp32 tensor of shape %s" % ((B, Hq, 1),))
+    return lib().attn_fwd_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), max_seqlen,
+                                  _ptr(o), _ptr(lse), B, Hq, Hkv, d, float(scale), int(chunk),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+
+
+def attn_get_device_status(stream=None):
+    return lib().attn_get_device_status(_stream_handle(stream))
+
+
+# --------------------------------------------------------------------------- convenience wrappers
+def forward(q, k, v, causal, scale, stream=None):
+    """Allocates O and LSE with torch on q's device and runs attn_fwd. Returns (o, lse)."""
+    B, Nq, Hq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    rc = attn_fwd(q, k, v, o, lse, causal, scale, stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def decode(q, k_cache, v_cache, seqlens, scale, chunk=1024, workspace=None, stream=None):
+    """Allocates O, LSE (and the workspace unless given) and runs attn_fwd_splitkv."""
+    B, _, Hq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = attn_splitkv_workspace_size(B, Hq, k_cache.shape[1], d, chunk)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    rc = attn_fwd_splitkv(q, k_cache, v_cache, seqlens, o, lse, scale, chunk, workspace, stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_splitkv")
+    return o, lse

@@ -1,0 +1,42 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Internal to the library.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Device status codes.  Kernels never trap: a wait that runs out of time
+// records (site << 8) | code in the unit's status word and the kernel unwinds.
+enum DeviceCode : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBadSeqlen = 6 };
+
+struct PrefillParams {
+  CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, N, B}, box {64, 1, 128, 1}, 128-B swizzle
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, Nq, Nk, d, causal;
+  float scale_log2;  // scale * log2(e)
+};
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+
+struct DecodeParams {
+  CUtensorMap tm_k, tm_v;  // 4-D maps {d, Hkv, max_seqlen, B}, box {64, 1, 64, 1}, 128-B swizzle
+  const void* q;
+  const int* seqlens;
+  void* o;
+  float* lse;
+  float* o_part;    // [B, Hq, n_split, d]
+  float* lse_part;  // [B, Hq, n_split]
+  int B, Hq, Hkv, d, max_seqlen, chunk, n_split;
+  float scale_log2;
+};
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// Reads and clears the device status word of each kernel unit (stream-ordered,
+// then synchronises the stream).  Returns the first non-zero word, or 0.
+cudaError_t fetch_status_prefill(cudaStream_t stream, uint32_t* out);
+cudaError_t fetch_status_decode(cudaStream_t stream, uint32_t* out);
+
+}  // namespace attn

@@ -1,0 +1,132 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact attention forward library
+ * (libattn_sm103.so).
+ *
+ * What is computed.  For query row i of head hq in batch b:
+ *     O[b,i,hq,:] = sum_j P_ij V[b,j,hkv,:],   P_ij = exp(s_ij - LSE_i),
+ *     s_ij = scale * <Q[b,i,hq,:], K[b,j,hkv,:]>   (-inf where masked),
+ *     LSE_i = ln sum_j exp(s_ij),
+ * i.e. O = softmax(scale * Q K^T + mask) V plus the per-row natural-log
+ * log-sum-exp ("FlashAttention: Part 2", chizkidd.github.io, section 2.1
+ * for the function and section 1.3 for the one LSE per row).  The result is
+ * reached by tiling over K/V blocks with a running max and sum (same page,
+ * section 6.2); the N x N score matrix is never written to memory.
+ *
+ * Grouped heads: Hkv divides Hq and query head hq reads KV head
+ * hq / (Hq / Hkv) (pyshine.com flash-attention tour, "Why You Need This":
+ * K and V may carry fewer heads than Q when the counts divide).
+ * Causal masking is aligned top-left: key j is visible to row i iff j <= i.
+ * A row that sees no key gets O = 0 and LSE = -inf.
+ *
+ * Layout: every tensor is dense and row-major, BSHD with d innermost:
+ *     q, o : [B, Nq, Hq, d]  bf16
+ *     k, v : [B, Nk, Hkv, d] bf16
+ *     lse  : [B, Hq, Nq]     fp32
+ * Supported head dims: d = 64 and d = 128.
+ *
+ * Ownership: every pointer is device memory owned by the caller.  The
+ * library allocates nothing and keeps no pointer after a call returns.
+ * Every call is asynchronous on the given stream (a cudaStream_t passed as
+ * void*, NULL for the legacy default stream); nothing synchronises except
+ * attn_get_device_status.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a
+ * failed check returns its code and launches nothing.  No exception crosses
+ * this interface.  Problems only the device can see (a pipeline wait that
+ * ran out of time, a cache length outside [0, max_seqlen]) are recorded in
+ * a library-wide device status word that attn_get_device_status reports.
+ */
+#ifndef ATTN_SM103_H
+#define ATTN_SM103_H
+
+#include <stddef.h>
+
+/* Exported symbols of the shared library (everything else is hidden). */
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* a size, head count, scale or pointer is invalid */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid but not built: d not in {64, 128}, ... */
+  ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
+  ATTN_ERR_LAUNCH = 4,       /* the CUDA runtime refused a launch or a query */
+  ATTN_ERR_TIMEOUT = 5,      /* device: a pipeline wait gave up (reported later) */
+  ATTN_ERR_DEVICE_ARG = 6,   /* device: a cache length was outside [0, max_seqlen] */
+  ATTN_ERR_WORKSPACE = 7     /* workspace missing or smaller than required */
+} attn_status;
+
+/*
+ * Prefill / training-shape forward.
+ *   q [B,Nq,Hq,d], k and v [B,Nk,Hkv,d] bf16 in; o [B,Nq,Hq,d] bf16 and
+ *   lse [B,Hq,Nq] fp32 out.  causal: 0 or 1 (top-left aligned).
+ *   scale: finite softmax scale applied to Q K^T (1/sqrt(d) usually).
+ * Tiled over 128-row query tiles and 128-key K/V tiles: TMA loads into
+ * shared memory, tcgen05 MMAs accumulate S = Q K^T and O += P V in Tensor
+ * Memory, the softmax runs on CUDA cores with an online running max/sum
+ * ("FlashAttention: Part 2", section 6.2), normalisation is deferred to the
+ * end and the O rescale is skipped when a row's max did not move
+ * ("Trace FlashAttention's evolution through plain PyTorch code", FA2 and
+ * FA4 paragraphs); key tiles wholly above the causal diagonal are skipped.
+ * Constraints: B, Hq, Hkv >= 1; Nq >= 0; Nk >= 0; Hq % Hkv == 0;
+ * d in {64, 128}; all pointers 16-byte aligned (lse: 4-byte) and non-NULL
+ * unless B*Nq == 0.  Sizes must keep every tensor below 2^31 rows.
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                     int causal, float scale, void* stream);
+
+/*
+ * Bytes of workspace attn_fwd_splitkv needs: fp32 partial outputs and
+ * partial LSEs for ceil(max_seqlen / chunk) splits of every (b, hq).
+ * Returns 0 for invalid arguments.
+ */
+ATTN_API size_t attn_splitkv_workspace_size(int B, int Hq, int max_seqlen, int d, int chunk);
+
+/*
+ * Query-length-one decode against a KV cache, split over the key axis
+ * (pyshine.com flash-attention tour, "Why You Need This": with one query
+ * the cache is split across thread blocks and the partial results are
+ * combined).
+ *   q [B,1,Hq,d] bf16; k_cache, v_cache [B,max_seqlen,Hkv,d] bf16;
+ *   seqlens: device int32 [B], valid cache length of each sequence
+ *            (keys 0 .. seqlens[b]-1 are attended; nothing at or beyond
+ *            seqlens[b] is read into the result, whatever it holds);
+ *   o [B,1,Hq,d] bf16 and lse [B,Hq,1] fp32 out;
+ *   chunk: keys per split, a positive multiple of 64 (1024 typical);
+ *   workspace: device memory of at least
+ *            attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk) bytes,
+ *            16-byte aligned, owned by the caller, contents ignored on entry.
+ * Two launches on `stream`: the split kernel writes each split's
+ * normalised partial output and LSE to the workspace, the combine kernel
+ * merges them.  A seqlens entry outside [0, max_seqlen] is clamped and
+ * reported as ATTN_ERR_DEVICE_ARG by attn_get_device_status.
+ */
+ATTN_API attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                             const int* seqlens, int max_seqlen,
+                             void* o, float* lse,
+                             int B, int Hq, int Hkv, int d, float scale, int chunk,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_ARG, or
+ * ATTN_ERR_LAUNCH if the stream itself reports an error.
+ */
+ATTN_API attn_status attn_get_device_status(void* stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+ATTN_API const char* attn_status_string(attn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SM103_H */

@@ -1,0 +1,88 @@
+"""The C-ABI library builds, loads and exports every function include/attn.h
+declares; host-side argument checks return their codes (no GPU needed: every
+call here fails validation before any CUDA call)."""
+import ctypes
+
+import pytest
+
+from exact_io_aware_14_gb300 import build as native_build
+from exact_io_aware_14_gb300 import _native
+
+
+@pytest.fixture(scope="module")
+def L():
+    native_build.build()
+    return _native.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _native.declared_functions()
+    for n in ("attn_fwd", "attn_fwd_splitkv", "attn_splitkv_workspace_size", "attn_get_device_status",
+              "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _native.declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_only_the_boundary_is_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _native.LIB_PATH], capture_output=True, text=True).stdout
+    ours = sorted({ln.split()[-1] for ln in out.splitlines() if " T attn_" in ln})
+    assert ours == _native.declared_functions()
+
+
+def test_status_strings(L):
+    for code in range(8):
+        s = _native.status_string(code)
+        assert s and s != "unknown status"
+    assert _native.status_string(99) == "unknown status"
+
+
+def _fwd(L, **kw):
+    a = dict(q=16, k=16, v=16, o=16, lse=16, B=1, Hq=2, Hkv=2, Nq=8, Nk=8, d=64, causal=0, scale=0.125)
+    a.update(kw)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.attn_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["o"]), vp(a["lse"]), a["B"], a["Hq"], a["Hkv"],
+                      a["Nq"], a["Nk"], a["d"], a["causal"], a["scale"], None)
+
+
+def test_attn_fwd_argument_checks(L):
+    assert _fwd(L, Hq=3, Hkv=2) == 1          # heads do not divide
+    assert _fwd(L, B=0) == 1
+    assert _fwd(L, Nq=-1) == 1
+    assert _fwd(L, causal=2) == 1
+    assert _fwd(L, scale=float("nan")) == 1
+    assert _fwd(L, scale=float("inf")) == 1
+    assert _fwd(L, d=96) == 2                 # not built
+    assert _fwd(L, q=0) == 1                  # NULL
+    assert _fwd(L, q=8) == 3                  # misaligned
+    assert _fwd(L, lse=2) == 3
+    assert _fwd(L, Nq=0) == 0                 # empty: nothing to do
+
+
+def _splitkv(L, **kw):
+    a = dict(q=16, k=16, v=16, s=16, S=2048, o=16, lse=16, B=2, Hq=8, Hkv=2, d=128, scale=0.1, chunk=1024,
+             ws=16, wsb=1 << 30)
+    a.update(kw)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.attn_fwd_splitkv(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["s"]), a["S"], vp(a["o"]), vp(a["lse"]),
+                              a["B"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["chunk"], vp(a["ws"]), a["wsb"],
+                              None)
+
+
+def test_splitkv_argument_checks(L):
+    assert _splitkv(L, Hq=6, Hkv=4) == 1
+    assert _splitkv(L, chunk=1000) == 1       # not a multiple of the 64-key tile
+    assert _splitkv(L, chunk=0) == 1
+    assert _splitkv(L, S=0) == 1
+    assert _splitkv(L, d=80) == 2
+    assert _splitkv(L, s=0) == 1
+    assert _splitkv(L, k=24) == 3
+    assert _splitkv(L, ws=0) == 7
+    need = L.attn_splitkv_workspace_size(2, 8, 2048, 128, 1024)
+    assert need == 2 * 8 * 2 * 128 * 4 + 2 * 8 * 2 * 4
+    assert _splitkv(L, wsb=need - 1) == 7
+    assert L.attn_splitkv_workspace_size(2, 8, 2048, 128, 1000) == 0
