@@ -49,6 +49,8 @@ def lib():
         L.attn_splitkv_workspace_size.argtypes = [i, i, i, i, i]
         L.attn_fwd_splitkv.restype = i
         L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+        L.attn_fwd_splitkv_noalloc.restype = i
+        L.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp]
         L.attn_get_device_status.restype = i
         L.attn_get_device_status.argtypes = [vp]
         L.attn_status_string.restype = ctypes.c_char_p
@@ -112,6 +114,25 @@ def attn_fwd_splitkv(q, k_cache, v_cache, seqlens, o, lse, scale, chunk, workspa
                                   _ptr(o), _ptr(lse), B, Hq, Hkv, d, float(scale), int(chunk),
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream_handle(stream))
+
+
+def attn_fwd_splitkv_noalloc(q, k_cache, v_cache, seqlens, o, lse, scale, chunk, stream=None):
+    """attn_fwd_splitkv without a workspace: the library's fixed device scratch
+    holds the partials, so nothing is allocated (for callers that cannot
+    allocate device memory).  Returns the status."""
+    B, _, Hq, d = q.shape
+    max_seqlen, Hkv = k_cache.shape[1], k_cache.shape[2]
+    _check_bf16("q", q, (B, 1, Hq, d))
+    _check_bf16("k_cache", k_cache, (B, max_seqlen, Hkv, d))
+    _check_bf16("v_cache", v_cache, (B, max_seqlen, Hkv, d))
+    _check_bf16("o", o, (B, 1, Hq, d))
+    if seqlens.dtype != torch.int32 or not seqlens.is_cuda or tuple(seqlens.shape) != (B,):
+        raise ValueError("seqlens must be a CUDA int32 tensor of shape (%d,)" % B)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, Hq, 1):
+        raise ValueError("lse must be a CUDA fp32 tensor of shape %s" % ((B, Hq, 1),))
+    return lib().attn_fwd_splitkv_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), max_seqlen,
+                                          _ptr(o), _ptr(lse), B, Hq, Hkv, d, float(scale), int(chunk),
+                                          _stream_handle(stream))
 
 
 def attn_get_device_status(stream=None):

@@ -116,6 +116,38 @@ ATTN_API attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const 
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Split-KV decode that allocates nothing, for callers that cannot call
+ * cudaMalloc or pass a workspace: code running inside a custom allocator or
+ * memory-pool callback, under a strict no-allocation policy of an inference
+ * server's hot loop, or behind a plain C interface with no device memory of
+ * its own to spare.  The paper has no counterpart to this entry point.
+ *
+ * Same arguments and results as attn_fwd_splitkv, minus the workspace: the
+ * partial results go to a fixed scratch array compiled into the library,
+ * ATTN_SPLITKV_NOALLOC_MAX_BYTES (8 MiB) in size, which every GPU that loads
+ * the library holds until the process exits.  That covers, for example,
+ * B=16, Hq=32, d=128, max_seqlen=16384, chunk=1024 (about 4.2 MB).
+ *   - Returns ATTN_ERR_WORKSPACE, launching nothing, when
+ *     attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk) exceeds the
+ *     scratch size; other argument errors are those of attn_fwd_splitkv.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device (with that device current) looks up the
+ *     scratch's device address once; make that first call before any stream
+ *     capture.  Returns ATTN_ERR_LAUNCH if the lookup fails.
+ *   - Every call on a device shares the one scratch array, which keeps the
+ *     last call's contents (nothing needs clearing: each call writes every
+ *     partial it reads).  Calls whose kernels may overlap on the GPU (on
+ *     different streams with no ordering between them) race on it: order
+ *     them on one stream or with events.
+ */
+#define ATTN_SPLITKV_NOALLOC_MAX_BYTES (8u << 20)
+ATTN_API attn_status attn_fwd_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                              const int* seqlens, int max_seqlen,
+                                              void* o, float* lse,
+                                              int B, int Hq, int Hkv, int d, float scale, int chunk,
+                                              void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word.  Returns ATTN_OK, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE_ARG, or
  * ATTN_ERR_LAUNCH if the stream itself reports an error.
