@@ -49,6 +49,30 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def profiled_traffic(workload_name):
+    """DRAM bytes per launch of the dominant kernel from the ncu summary under
+    profiles/, or None when there is none or the kernel source changed since."""
+    import glob
+    import hashlib
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith((" ", "|", "#")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("workload") != workload_name or "traffic_bytes_per_launch" not in fields:
+            continue
+        src, _, sha = fields.get("kernel_source", "").partition(" sha256:")
+        try:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                cur = hashlib.sha256(f.read()).hexdigest()[:16]
+        except OSError:
+            return None
+        return int(fields["traffic_bytes_per_launch"]) if cur == sha else None
+    return None
+
+
 # --------------------------------------------------------------------------- clocks (NVML via ctypes)
 class ClockSampler:
     """Samples SM clock and clock-event reasons every few ms while running."""
@@ -328,14 +352,14 @@ def run_ours(args, w, rank, world, local_rank):
     if dec:
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "achieved": kernel_rate, "peak": peak, "unit": "GB/s",
-                "frac": kernel_rate / peak, "traffic": None,
+                "frac": kernel_rate / peak, "traffic": profiled_traffic(w.name),
                 "peak_source": "%s hbm_gbs (copy)" % peak_src,
                 "kernel": "decode split + combine (one step, both launches)",
                 "algorithmic_bytes_per_step": work}
     else:
         peak = float(peaks["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": kernel_rate, "peak": peak, "unit": "TFLOP/s",
-                "frac": kernel_rate / peak, "traffic": None,
+                "frac": kernel_rate / peak, "traffic": profiled_traffic(w.name),
                 "peak_source": "%s bf16_tflops (burst cuBLAS)" % peak_src,
                 "kernel": "prefill_fwd_kernel<%d>" % w.d, "algorithmic_flops_per_launch": work}
 
