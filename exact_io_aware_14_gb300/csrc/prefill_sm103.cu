@@ -1,23 +1,33 @@
 // Exact attention forward, prefill / training shapes, for sm_103a.
 //
-// One CTA computes one 128-row query tile of one (batch, query head):
-//   warp 0      TMA producer: Q once, then K_j / V_j tiles into a ring
-//   warp 1      TMEM allocator and MMA issuer (one thread):
-//                 S_j = Q K_j^T  -> TMEM (two S buffers, so QK^T of tile j+1
-//                                   overlaps the softmax of tile j)
-//                 O  += P_j V_j  -> TMEM
-//   warps 2-5   softmax: one thread owns one query row (TMEM lane), keeps
-//               the running max m and sum l in registers, writes P_j (bf16)
-//               to shared memory, rescales its O row only when m moved,
-//               and at the end writes O / l and the row's LSE.
+// One CTA computes two 128-row query tiles that share every K/V tile: two
+// consecutive row tiles of one head, or -- when the GQA group size is even --
+// the same row tile of two query heads that read the same KV head (equal
+// causal extents).  Twelve warps:
+//   warp 0        TMA producer: Q0, Q1 once, then K_j / V_j into rings
+//   warp 1        TMEM allocator and MMA issuer (one thread), per key tile j:
+//                   O_0 += P_0 V_{j-1};  S_0 = Q_0 K_j^T;
+//                   O_1 += P_1 V_{j-1};  S_1 = Q_1 K_j^T
+//                 so the tensor core works on one tile while the softmax
+//                 warpgroup of the other tile runs (ping-pong).
+//   warps 4-7     softmax of tile 0, warps 8-11 softmax of tile 1: one
+//                 thread owns one query row (one TMEM lane); it reads its
+//                 128 scores, updates the running max m and sum l, rescales
+//                 its O row in TMEM only if m moved, and writes P (bf16)
+//                 back into TMEM over the scores; the P.V MMA reads P from
+//                 TMEM as its A operand.  At the end: O / l and the LSE.
+//
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
+// O_1 [384,384+d); P_t is packed bf16x2 in the first 64 columns of S_t.
 //
 // The method is the tiled online softmax of "FlashAttention: Part 2"
 // (chizkidd.github.io), section 6.2: per score tile, update (m, l, a) with
 // alpha = exp(m - m') and discard the tile.  Normalisation is deferred to the
 // epilogue and the rescale is skipped when the max did not move ("Trace
 // FlashAttention's evolution through plain PyTorch code", FA2 and FA4
-// paragraphs).  Scores are handled in base 2: t = s * scale * log2(e), so
-// p = 2^(t - m) and LSE = (m + log2 l) * ln 2.
+// paragraphs); the two-tile ping-pong follows the FA3 schedule of section 1.5.
+// Scores are handled in base 2: p = 2^(s*c - m*c) with c = scale*log2(e) folded
+// into one FMA, and LSE = (m*c + log2 l) * ln 2.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,23 +41,21 @@ __device__ uint32_t g_prefill_status;
 
 constexpr int BM = 128;  // query rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;  // keys per K/V tile (MMA N of QK^T, K of PV)
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: no legitimate wait comes close
-constexpr uint32_t kTmemCols = 512;               // S0 [0,128) S1 [128,256) O [256, 256+d)
+constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct Layout {
-  static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kHalf = BM * 128;            // one 64-column block of a 128-row tile
-  static constexpr int kQBytes = BM * D * 2;
-  static constexpr int kKVBytes = BN * D * 2;
-  static constexpr int kPBytes = BM * BN * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffP = kOffV + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
-  static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 1 + 1;
+  static constexpr int kKStages = (D == 64) ? 3 : 2;
+  static constexpr int kVStages = (D == 64) ? 3 : 2;
+  static constexpr int kHalf = 128 * 128;  // one 64-column block of a 128-row tile
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kOffQ = 0;  // Q_0, Q_1
+  static constexpr int kOffK = kOffQ + 2 * kTile;
+  static constexpr int kOffV = kOffK + kKStages * kTile;
+  static constexpr int kOffBar = kOffV + kVStages * kTile;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -73,57 +81,80 @@ __device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, volatil
   return ok;
 }
 
+struct TileInfo {
+  int hq;    // query head
+  int row0;  // first query row
+  int n_kt;  // key tiles this tile visits (0: inactive)
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                        float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
-                       float scale_log2, int n_qtiles) {
+                       float scale_log2, int pair_heads, int units_per_bh) {
   using L = Layout<D>;
-  constexpr int S = L::kStages;
+  constexpr int KS = L::kKStages;
+  constexpr int VS = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* bar_q = bars;
   uint64_t* bar_kfull = bars + 1;
-  uint64_t* bar_vfull = bar_kfull + S;
-  uint64_t* bar_kvempty = bar_vfull + S;
-  uint64_t* bar_sfull = bar_kvempty + S;  // [2]
-  uint64_t* bar_sfree = bar_sfull + 2;    // [2]
-  uint64_t* bar_pfull = bar_sfree + 2;
-  uint64_t* bar_odone = bar_pfull + 1;
+  uint64_t* bar_kempty = bar_kfull + KS;
+  uint64_t* bar_vfull = bar_kempty + KS;
+  uint64_t* bar_vempty = bar_vfull + VS;
+  uint64_t* bar_sfull = bar_vempty + VS;  // [2]
+  uint64_t* bar_pfull = bar_sfull + 2;    // [2]
+  uint64_t* bar_odone = bar_pfull + 2;    // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: longest causal tiles first (the block scheduler issues low ids first).
-  const int bh_count = B * Hq;
-  const int qt_rev = blockIdx.x / bh_count;
+  // ---- work unit: (unit index, head slot, batch); longest causal units first
+  const int hslots = pair_heads ? Hq / 2 : Hq;
+  const int bh_count = B * hslots;
+  const int u_rev = blockIdx.x / bh_count;
   const int bh = blockIdx.x % bh_count;
-  const int qt = causal ? (n_qtiles - 1 - qt_rev) : qt_rev;
-  const int b = bh / Hq;
-  const int hq = bh % Hq;
-  const int hkv = hq / (Hq / Hkv);
-  const int row0 = qt * BM;
-  const int kend = causal ? min(Nk, row0 + BM) : Nk;
-  const int n_kt = (kend + BN - 1) / BN;
+  const int unit = causal ? (units_per_bh - 1 - u_rev) : u_rev;
+  const int b = bh / hslots;
+  const int hs = bh % hslots;
+  TileInfo ti[2];
+  if (pair_heads) {
+    ti[0].hq = 2 * hs;
+    ti[1].hq = 2 * hs + 1;
+    ti[0].row0 = ti[1].row0 = unit * BM;
+  } else {
+    ti[0].hq = ti[1].hq = hs;
+    ti[0].row0 = (2 * unit) * BM;
+    ti[1].row0 = (2 * unit + 1) * BM;
+  }
+  const int hkv = ti[0].hq / (Hq / Hkv);  // both heads of a pair share the KV head
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int kend = causal ? min(Nk, ti[t].row0 + BM) : Nk;
+    ti[t].n_kt = (ti[t].row0 < Nq) ? (kend + BN - 1) / BN : 0;
+  }
+  const int n_kt = max(ti[0].n_kt, ti[1].n_kt);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(bar_kfull + s, 1);
+      mbar_init(bar_kempty + s, 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(bar_vfull + s, 1);
-      mbar_init(bar_kvempty + s, 1);
+      mbar_init(bar_vempty + s, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_sfull + i, 1);
-      mbar_init(bar_sfree + i, 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_sfull + t, 1);
+      mbar_init(bar_pfull + t, 128);
+      mbar_init(bar_odone + t, 1);
     }
-    mbar_init(bar_pfull, 128);
-    mbar_init(bar_odone, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -135,12 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
 
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
-  uint8_t* sP = smem + L::kOffP;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -148,17 +177,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar_q, L::kQBytes);
-      for (int h = 0; h < D / 64; ++h) tma_load_4d(sQ + h * L::kHalf, &tm_q, bar_q, h * 64, hq, row0, b);
-      for (int j = 0; j < n_kt; ++j) {
-        const int s = j % S;
-        if (j >= S && !wait_one(bar_kvempty + s, ((j / S) - 1) & 1, abort_flag, 1)) break;
-        mbar_arrive_expect_tx(bar_kfull + s, L::kKVBytes);
+      mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
+      for (int t = 0; t < 2; ++t)
         for (int h = 0; h < D / 64; ++h)
-          tma_load_4d(sK + s * L::kKVBytes + h * L::kHalf, &tm_k, bar_kfull + s, h * 64, hkv, j * BN, b);
-        mbar_arrive_expect_tx(bar_vfull + s, L::kKVBytes);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_4d(sV + s * L::kKVBytes + h * L::kHalf, &tm_v, bar_vfull + s, h * 64, hkv, j * BN, b);
+          tma_load_4d(sQ + t * L::kTile + h * L::kHalf, &tm_q, bar_q, h * 64, ti[t].hq, ti[t].row0, b);
+      // K_j is consumed at MMA step j, V_{j-1} at step j: load in that order
+      for (int j = 0; j <= n_kt; ++j) {
+        if (j < n_kt) {
+          const int s = j % KS;
+          if (j >= KS && !wait_one(bar_kempty + s, ((j / KS) - 1) & 1, abort_flag, 1)) break;
+          mbar_arrive_expect_tx(bar_kfull + s, L::kTile);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_kfull + s, h * 64, hkv, j * BN, b);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj % VS;
+          if (jj >= VS && !wait_one(bar_vempty + s, ((jj / VS) - 1) & 1, abort_flag, 2)) break;
+          mbar_arrive_expect_tx(bar_vfull + s, L::kTile);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_vfull + s, h * 64, hkv, jj * BN, b);
+        }
       }
     }
   } else if (warp == 1) {
@@ -166,138 +204,154 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kt > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
-      bool ok = wait_one(bar_q, 0, abort_flag, 2);
-      auto issue_pv = [&](int t) -> bool {
-        const int s = t % S;
-        if (!wait_one(bar_pfull, t & 1, abort_flag, 3)) return false;
-        if (!wait_one(bar_vfull + s, (t / S) & 1, abort_flag, 4)) return false;
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      bool ok = wait_one(bar_q, 0, abort_flag, 3);
+      for (int j = 0; ok && j <= n_kt; ++j) {
+        const int ks = j % KS, vs = (j - 1 + VS) % VS;
+        if (j < n_kt && !wait_one(bar_kfull + ks, (j / KS) & 1, abort_flag, 4)) { ok = false; break; }
+        if (j >= 1 && !wait_one(bar_vfull + vs, ((j - 1) / VS) & 1, abort_flag, 5)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t da = sdesc_sw128(aP + (ks >> 2) * L::kHalf + (ks & 3) * 32, 16, 1024);
-          const uint64_t db = sdesc_sw128(aV + s * L::kKVBytes + ks * 16 * 128, L::kHalf, 1024);
-          mma_bf16_ss(tO, da, db, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-        }
-        mma_commit(bar_odone);
-        mma_commit(bar_kvempty + s);
-        return true;
-      };
-      for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j % S;
-        if (!wait_one(bar_kfull + s, (j / S) & 1, abort_flag, 5)) { ok = false; break; }
-        if (j >= 2 && !wait_one(bar_sfree + (j & 1), ((j >> 1) - 1) & 1, abort_flag, 6)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t tS = (j & 1) ? tS1 : tS0;
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t tS = tmem + t * 128;
+          const uint32_t tO = tmem + 256 + t * 128;
+          if (j >= 1 && j - 1 < ti[t].n_kt) {
+            // O_t += P_t V_{j-1}; P_t sits in the first 64 columns of S_t
+            if (!wait_one(bar_pfull + t, (j - 1) & 1, abort_flag, 6)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t da = sdesc_sw128(aQ + (ks >> 2) * L::kHalf + (ks & 3) * 32, 16, 1024);
-          const uint64_t db = sdesc_sw128(aK + s * L::kKVBytes + (ks >> 2) * L::kHalf + (ks & 3) * 32, 16, 1024);
-          mma_bf16_ss(tS, da, db, idesc_qk, ks > 0 ? 1u : 0u);
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t db = sdesc_sw128(aV + vs * L::kTile + kk * 16 * 128, L::kHalf, 1024);
+              mma_bf16_ts(tO, tS + kk * 8, db, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (j == ti[t].n_kt) mma_commit(bar_odone + t);
+          }
+          if (j < ti[t].n_kt) {
+            // S_t = Q_t K_j^T (after the P.V that read P_t: MMAs run in issue order)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t da = sdesc_sw128(aQ + t * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
+              const uint64_t db = sdesc_sw128(aK + ks * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
+              mma_bf16_ss(tS, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_sfull + t);
+          }
         }
-        mma_commit(bar_sfull + (j & 1));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (!ok) break;
+        if (j < n_kt) mma_commit(bar_kempty + ks);
+        if (j >= 1) mma_commit(bar_vempty + vs);
       }
-      if (ok) issue_pv(n_kt - 1);
     }
-  } else {
+  } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax
+    const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+    const TileInfo me = t ? ti[1] : ti[0];
     const int quarter = warp & 3;  // TMEM lanes this warp may touch: 32*quarter .. +31
     const int r = quarter * 32 + lane;
-    const int grow = row0 + r;
+    const int grow = me.row0 + r;
+    const int my_kt = me.n_kt;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t sP_row = smem_u32(sP) + r * 128;
-    float m = -INFINITY;  // running max, base-2 scaled units
-    float l = 0.f;        // running sum of 2^(t - m)
+    const uint32_t tS = tmem + t * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + t * 128 + lane_off;
+    // with a negative scale, work on -s with |c| so the max logic is unchanged
+    const bool negate = scale_log2 < 0.f;
+    const float c = negate ? -scale_log2 : scale_log2;
+    float m = -INFINITY;  // running max of the (sign-adjusted) raw scores
+    float l = 0.f;        // running sum of 2^(s*c - m*c)
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      if (!wait_all(bar_sfull + (j & 1), (j >> 1) & 1, abort_flag, 7)) { ok = false; break; }
+    for (int j = 0; j < my_kt; ++j) {
+      if (!wait_all(bar_sfull + t, j & 1, abort_flag, 7)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off;
-      float t[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tS + c * 32, u);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) t[c * 32 + i] = __uint_as_float(u[i]);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar_sfree + (j & 1));
-
       const int kbase = j * BN;
-      float mt = -INFINITY;
-      if (kbase + BN > Nk || (causal && kbase + BN - 1 > row0)) {
-        int lim = Nk - kbase;
+      const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0);
+      int lim = BN;  // columns [lim, BN) of this tile are masked for this row
+      if (masked) {
+        lim = Nk - kbase;
         if (causal) lim = min(lim, grow - kbase + 1);
+      }
+      // pass 1: row max over the tile, 64 columns at a time
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          t[i] = (i < lim) ? t[i] * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, t[i]);
-        }
-      } else {
+      for (int h = 0; h < 2; ++h) {
+        uint32_t u[2][32];
+        tmem_ld32(tS + 64 * h, u[0]);
+        tmem_ld32(tS + 64 * h + 32, u[1]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          t[i] *= scale_log2;
-          mt = fmaxf(mt, t[i]);
+        for (int i = 0; i < 64; ++i) {
+          float v = __uint_as_float(u[i >> 5][i & 31]);
+          if (negate) v = -v;
+          if (masked && 64 * h + i >= lim) v = -INFINITY;
+          mx[i & 3] = fmaxf(mx[i & 3], v);
         }
       }
-      const float m_new = fmaxf(m, mt);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      float rsum = 0.f;
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+      const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
+      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(fmaf(m, c, -mc));
+      // pass 2: p = 2^(s*c - m*c), row sum, P (bf16 pairs) into the first 64
+      // columns of S_t; half h of P only overwrites scores already consumed
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t u[2][32];
+        tmem_ld32(tS + 64 * h, u[0]);
+        tmem_ld32(tS + 64 * h + 32, u[1]);
+        tmem_wait_ld();
+        uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        t[i] = ex2_approx(t[i] - m_use);
-        rsum += t[i];
-      }
-      const float alpha = ex2_approx(m - m_use);  // m = -inf -> 0
-      l = l * alpha + rsum;
-
-      if (j > 0) {
-        // O holds the sum through tile j-1 once PV_{j-1} completes; P's buffer is free then too
-        if (!wait_all(bar_odone, (j - 1) & 1, abort_flag, 8)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, m_new != m)) {
-          const float a = (m_new != m) ? alpha : 1.f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32(tO + lane_off + c * 32, u);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
-            tmem_st32(tO + lane_off + c * 32, u);
+        for (int i = 0; i < 32; ++i) {
+          float v0 = __uint_as_float(u[i >> 4][(2 * i) & 31]);
+          float v1 = __uint_as_float(u[i >> 4][(2 * i + 1) & 31]);
+          if (negate) {
+            v0 = -v0;
+            v1 = -v1;
           }
-          tmem_wait_st();
+          float p0 = ex2_approx(fmaf(v0, c, -mc));
+          float p1 = ex2_approx(fmaf(v1, c, -mc));
+          if (masked) {  // also covers c == 0, where -inf * 0 would not give 0
+            p0 = (64 * h + 2 * i < lim) ? p0 : 0.f;
+            p1 = (64 * h + 2 * i + 1 < lim) ? p1 : 0.f;
+          }
+          sm[(2 * i) & 3] += p0;
+          sm[(2 * i + 1) & 3] += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + 32 * h, pk);
+      }
+      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+
+      // O_t holds the sum through tile j-1 (P.V of j-1 completed before S_j was
+      // written): rescale it now if this row's max moved.
+      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+        const float a = (m_new != m) ? alpha : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t u[32];
+          tmem_ld32(tO + cc * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
+          tmem_st32(tO + cc * 32, u);
         }
       }
       m = m_new;
-
-      // P row -> shared memory, K-major with the 128-B swizzle the MMA descriptor expects
-#pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        const uint32_t addr = sP_row + (c >> 3) * L::kHalf + ((((c & 7) ^ (r & 7))) << 4);
-        st_shared_v4(addr, pack_bf16x2(t[8 * c + 0], t[8 * c + 1]), pack_bf16x2(t[8 * c + 2], t[8 * c + 3]),
-                     pack_bf16x2(t[8 * c + 4], t[8 * c + 5]), pack_bf16x2(t[8 * c + 6], t[8 * c + 7]));
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_pfull);
+      mbar_arrive(bar_pfull + t);
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (ok && n_kt > 0) ok = wait_all(bar_odone, (n_kt - 1) & 1, abort_flag, 9);
-    if (ok) {
+    if (ok && my_kt > 0) ok = wait_all(bar_odone + t, 0, abort_flag, 8);
+    if (ok && me.row0 < Nq) {
       tc_fence_after();
       const bool store = grow < Nq;
-      __nv_bfloat16* orow = out + ((static_cast<size_t>(b) * Nq + grow) * Hq + hq) * D;
+      __nv_bfloat16* orow = out + ((static_cast<size_t>(b) * Nq + grow) * Hq + me.hq) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t u[32];
-        if (n_kt > 0) {
-          tmem_ld32(tO + lane_off + c * 32, u);
+        if (my_kt > 0) {
+          tmem_ld32(tO + cc * 32, u);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -308,14 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i)
           w[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
       if (store) {
-        const float lse = (l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-        lse_out[(static_cast<size_t>(b) * Hq + hq) * Nq + grow] = lse;
+        const float lse = (l > 0.f) ? (m * c + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        lse_out[(static_cast<size_t>(b) * Hq + me.hq) * Nq + grow] = lse;
       }
     }
   }
@@ -333,14 +387,18 @@ template <int D>
 cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
   using L = Layout<D>;
   const int n_qtiles = (p.Nq + BM - 1) / BM;
-  const long long blocks = static_cast<long long>(n_qtiles) * p.B * p.Hq;
+  const int G = p.Hq / p.Hkv;
+  const int pair_heads = (G % 2 == 0) ? 1 : 0;
+  const int units_per_bh = pair_heads ? n_qtiles : (n_qtiles + 1) / 2;
+  const int hslots = pair_heads ? p.Hq / 2 : p.Hq;
+  const long long blocks = static_cast<long long>(units_per_bh) * p.B * hslots;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(prefill_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   prefill_fwd_kernel<D><<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, stream>>>(
       p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.causal,
-      p.scale_log2, n_qtiles);
+      p.scale_log2, pair_heads, units_per_bh);
   return cudaGetLastError();
 }
 
