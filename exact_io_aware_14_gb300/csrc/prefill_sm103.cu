@@ -87,7 +87,80 @@ struct TileInfo {
   int n_kt;  // key tiles this tile visits (0: inactive)
 };
 
-template <int D>
+// The exponent reference of a row is moved (and O, l rescaled) only when the
+// tile max exceeds it by more than this many powers of two; until then p may
+// reach 2^8, which bf16 P, fp32 l and the fp32 O accumulator hold without loss
+// of range, and O / l and the LSE come out the same.
+constexpr float kRescaleLog2 = 8.f;
+
+// Row max of one 128-column score tile in TMEM (this thread's lane), read in
+// two 64-column halves.  kNeg: the scale is negative, work on -s.
+template <bool kMasked, bool kNeg>
+__device__ __forceinline__ float score_tile_max(uint32_t tS, int lim) {
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t u[2][32];
+    tmem_ld32(tS + 64 * h, u[0]);
+    tmem_ld32(tS + 64 * h + 32, u[1]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[k] = __uint_as_float(u[(i + k) >> 5][(i + k) & 31]);
+        if (kNeg) v[k] = -v[k];
+        if (kMasked) v[k] = (64 * h + i + k < lim) ? v[k] : -INFINITY;
+      }
+      mx0 = fmax3(mx0, v[0], v[1]);
+      mx1 = fmax3(mx1, v[2], v[3]);
+    }
+  }
+  return fmaxf(mx0, mx1);
+}
+
+// p = 2^(s*c - mc) for the 128 scores of this lane, written back as bf16
+// pairs over the first 64 columns (half h of P only overwrites scores already
+// consumed).  Returns the row sum of the fp32 p.
+template <bool kMasked, bool kNeg>
+__device__ __forceinline__ float score_tile_exp(uint32_t tS, int lim, float c, float mc) {
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+  const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    uint32_t u[2][32];
+    tmem_ld32(tS + 64 * h, u[0]);
+    tmem_ld32(tS + 64 * h + 32, u[1]);
+    tmem_wait_ld();
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float v0 = __uint_as_float(u[i >> 4][(2 * i) & 31]);
+      float v1 = __uint_as_float(u[i >> 4][(2 * i + 1) & 31]);
+      if (kNeg) {
+        v0 = -v0;
+        v1 = -v1;
+      }
+      const float2 x = ffma2(make_float2(v0, v1), c2, nmc2);
+      float p0 = ex2_approx(x.x);
+      float p1 = ex2_approx(x.y);
+      if (kMasked) {  // also right for c == 0, where -inf * 0 would not give 0
+        p0 = (64 * h + 2 * i < lim) ? p0 : 0.f;
+        p1 = (64 * h + 2 * i + 1 < lim) ? p1 : 0.f;
+      }
+      if (i & 1)
+        acc1 = fadd2(acc1, make_float2(p0, p1));
+      else
+        acc0 = fadd2(acc0, make_float2(p0, p1));
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(tS + 32 * h, pk);
+  }
+  return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+template <int D, bool kNeg>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
@@ -253,10 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + t * 128 + lane_off;
     const uint32_t tO = tmem + 256 + t * 128 + lane_off;
-    // with a negative scale, work on -s with |c| so the max logic is unchanged
-    const bool negate = scale_log2 < 0.f;
-    const float c = negate ? -scale_log2 : scale_log2;
-    float m = -INFINITY;  // running max of the (sign-adjusted) raw scores
+    // with a negative scale the kernel works on -s with |c| (kNeg), so the
+    // max logic is the same
+    const float c = kNeg ? -scale_log2 : scale_log2;
+    float m = -INFINITY;  // exponent reference of this row (sign-adjusted raw score units)
     float l = 0.f;        // running sum of 2^(s*c - m*c)
     bool ok = true;
     for (int j = 0; j < my_kt; ++j) {
@@ -269,68 +342,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         lim = Nk - kbase;
         if (causal) lim = min(lim, grow - kbase + 1);
       }
-      // pass 1: row max over the tile, 64 columns at a time
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t u[2][32];
-        tmem_ld32(tS + 64 * h, u[0]);
-        tmem_ld32(tS + 64 * h + 32, u[1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float v = __uint_as_float(u[i >> 5][i & 31]);
-          if (negate) v = -v;
-          if (masked && 64 * h + i >= lim) v = -INFINITY;
-          mx[i & 3] = fmaxf(mx[i & 3], v);
-        }
-      }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+      const float mt = masked ? score_tile_max<true, kNeg>(tS, lim) : score_tile_max<false, kNeg>(tS, lim);
+      // move the reference only on the first visible scores or when the tile
+      // max is more than 2^kRescaleLog2 above it
+      const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
+      const float m_new = need ? fmaxf(m, mt) : m;
       const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
-      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(fmaf(m, c, -mc));
-      // pass 2: p = 2^(s*c - m*c), row sum, P (bf16 pairs) into the first 64
-      // columns of S_t; half h of P only overwrites scores already consumed
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        uint32_t u[2][32];
-        tmem_ld32(tS + 64 * h, u[0]);
-        tmem_ld32(tS + 64 * h + 32, u[1]);
-        tmem_wait_ld();
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v0 = __uint_as_float(u[i >> 4][(2 * i) & 31]);
-          float v1 = __uint_as_float(u[i >> 4][(2 * i + 1) & 31]);
-          if (negate) {
-            v0 = -v0;
-            v1 = -v1;
-          }
-          float p0 = ex2_approx(fmaf(v0, c, -mc));
-          float p1 = ex2_approx(fmaf(v1, c, -mc));
-          if (masked) {  // also covers c == 0, where -inf * 0 would not give 0
-            p0 = (64 * h + 2 * i < lim) ? p0 : 0.f;
-            p1 = (64 * h + 2 * i + 1 < lim) ? p1 : 0.f;
-          }
-          sm[(2 * i) & 3] += p0;
-          sm[(2 * i + 1) & 3] += p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tS + 32 * h, pk);
-      }
-      l = l * alpha + ((sm[0] + sm[1]) + (sm[2] + sm[3]));
+      const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
+      const float rowsum = masked ? score_tile_exp<true, kNeg>(tS, lim, c, mc)
+                                  : score_tile_exp<false, kNeg>(tS, lim, c, mc);
+      l = l * alpha + rowsum;
 
       // O_t holds the sum through tile j-1 (P.V of j-1 completed before S_j was
-      // written): rescale it now if this row's max moved.
-      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
-        const float a = (m_new != m) ? alpha : 1.f;
+      // written): rescale it now if this row's reference moved.
+      if (j > 0 && __any_sync(0xffffffffu, need && m != -INFINITY)) {
+        const float a = (need && m != -INFINITY) ? alpha : 1.f;
+        const float2 a2 = make_float2(a, a);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t u[32];
           tmem_ld32(tO + cc * 32, u);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * a);
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = fmul2(make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), a2);
+            u[2 * i] = __float_as_uint(x.x);
+            u[2 * i + 1] = __float_as_uint(x.y);
+          }
           tmem_st32(tO + cc * 32, u);
         }
       }
@@ -394,9 +432,10 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(units_per_bh) * p.B * hslots;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(prefill_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  auto kern = (p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true> : prefill_fwd_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  prefill_fwd_kernel<D><<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, stream>>>(
+  kern<<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, stream>>>(
       p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.causal,
       p.scale_log2, pair_heads, units_per_bh);
   return cudaGetLastError();

@@ -40,8 +40,17 @@ def _visible(nq, nk, causal, kv_len):
 
 
 def online_attention(q, k, v, scale, causal=False, tile=64, kv_len=None,
-                     conditional_rescale=True, normalise_each_tile=False):
-    """Tiled online softmax over key tiles of ``tile`` keys. Returns (O, LSE)."""
+                     conditional_rescale=True, normalise_each_tile=False, rescale_threshold=None):
+    """Tiled online softmax over key tiles of ``tile`` keys. Returns (O, LSE).
+
+    ``rescale_threshold`` (natural-log units): when given, the exponent
+    reference m of a row is moved -- and l, a rescaled -- only when a tile's
+    max exceeds it by more than the threshold ("skip the rescale when the
+    running max doesn't need it", read as: while the exponentials stay within
+    a bounded range); otherwise the stale reference is kept and p may exceed 1.
+    """
+    if rescale_threshold is not None:
+        return _online_thresholded(q, k, v, scale, causal, tile, kv_len, rescale_threshold)
     nq, d = q.shape
     nk = k.shape[0]
     vis = _visible(nq, nk, causal, kv_len)
@@ -77,6 +86,35 @@ def online_attention(q, k, v, scale, causal=False, tile=64, kv_len=None,
     seen = l > 0
     with np.errstate(invalid="ignore", divide="ignore"):
         o = a if normalise_each_tile else np.where(seen[:, None], a / l[:, None], 0.0)
+        lse = np.where(seen, m + np.log(l), -np.inf)
+    return o, lse
+
+
+def _online_thresholded(q, k, v, scale, causal, tile, kv_len, threshold):
+    nq = q.shape[0]
+    nk = k.shape[0]
+    vis = _visible(nq, nk, causal, kv_len)
+    m = np.full(nq, -np.inf)          # exponent reference (may lag the true max)
+    l = np.zeros(nq)
+    a = np.zeros((nq, v.shape[1]))
+    for j0 in range(0, nk, tile):
+        j1 = min(nk, j0 + tile)
+        s = scale * (q @ k[j0:j1].T)
+        s = np.where(vis[:, j0:j1], s, -np.inf)
+        mt = s.max(axis=1)
+        with np.errstate(invalid="ignore"):
+            move = (m == -np.inf) | (mt - m > threshold)
+        m_new = np.where(move, np.maximum(m, mt), m)
+        seen = m_new > -np.inf
+        m_safe = np.where(seen, m_new, 0.0)
+        alpha = np.where(m == -np.inf, 0.0, np.where(move, np.exp(m - m_safe), 1.0))
+        p = np.exp(s - m_safe[:, None])
+        l = alpha * l + p.sum(axis=1)
+        a = alpha[:, None] * a + p @ v[j0:j1]
+        m = m_new
+    seen = l > 0
+    with np.errstate(invalid="ignore", divide="ignore"):
+        o = np.where(seen[:, None], a / l[:, None], 0.0)
         lse = np.where(seen, m + np.log(l), -np.inf)
     return o, lse
 

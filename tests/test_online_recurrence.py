@@ -54,6 +54,22 @@ def test_conditional_rescale_is_bitwise_identical_to_always_rescaling():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("threshold", [0.0, 8 * math.log(2), 40.0])
+@pytest.mark.parametrize("amp", [1.0, 12.0])
+def test_thresholded_reference_matches_naive(causal, threshold, amp):
+    """Keeping a stale exponent reference until the max rises by more than a
+    threshold reaches the same O and LSE (large amp forces moves)."""
+    q, k, v = _rand(40, 300, 16, seed=54)
+    qd = _head(q) * amp
+    qb = torch.from_numpy(qd).to(torch.bfloat16)[None, :, None, :]
+    o_ref, lse_ref = oracle.attn_fwd(qb, k, v, causal, 0.25)
+    o, lse = online.online_attention(qb[0, :, 0].double().numpy(), _head(k), _head(v), 0.25, causal, 32,
+                                     rescale_threshold=threshold)
+    np.testing.assert_allclose(o, o_ref[0, :, 0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref[0, 0], rtol=1e-14, atol=1e-12)
+
+
 def test_online_with_cache_length_and_empty_row():
     q, k, v = _rand(3, 50, 8, seed=51)
     for L in (0, 1, 17, 50):

@@ -63,6 +63,15 @@ def test_small_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
     _full_check(q, k, v, causal, 1 / math.sqrt(d), "B%d Hq%d Hkv%d Nq%d Nk%d d%d c%d" % (B, Hq, Hkv, Nq, Nk, d, causal))
 
 
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.5])
+def test_negative_zero_and_large_scale(scale):
+    """A negative scale runs the sign-flipped kernel variant; scale 0 gives
+    uniform weights (masked columns must still get exactly 0)."""
+    q, k, v = workloads.prefill_inputs(1, 4, 2, 300, 300, 128, seed=12)
+    for causal in (False, True):
+        _full_check(q, k, v, causal, scale, "scale %g causal=%d" % (scale, causal))
+
+
 def test_no_keys_gives_zero_and_minus_inf():
     q, k, v = workloads.prefill_inputs(1, 2, 2, 130, 0, 64, seed=7)
     o, lse = _run(q, k, v, False, 0.125)
