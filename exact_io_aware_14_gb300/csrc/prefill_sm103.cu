@@ -4,7 +4,8 @@
 // consecutive row tiles of one head, or -- when the GQA group size is even --
 // the same row tile of two query heads that read the same KV head (equal
 // causal extents).  Twelve warps:
-//   warp 0        TMA producer: Q0, Q1 once, then K_j / V_j into rings
+//   warp 0        TMA producer: Q0, Q1 once, then K/V tiles into one ring of
+//                 shared-memory slots in the order the MMA thread uses them
 //   warp 1        TMEM allocator and MMA issuer (one thread), per key tile j:
 //                   O_0 += P_0 V_{j-1};  S_0 = Q_0 K_j^T;
 //                   O_1 += P_1 V_{j-1};  S_1 = Q_1 K_j^T
@@ -47,15 +48,14 @@ constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct Layout {
-  static constexpr int kKStages = (D == 64) ? 3 : 2;
-  static constexpr int kVStages = (D == 64) ? 3 : 2;
+  // one ring of K and V tiles, filled in the order the MMA thread uses them
+  static constexpr int kSlots = (D == 64) ? 10 : 5;
   static constexpr int kHalf = 128 * 128;  // one 64-column block of a 128-row tile
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kOffQ = 0;  // Q_0, Q_1
-  static constexpr int kOffK = kOffQ + 2 * kTile;
-  static constexpr int kOffV = kOffK + kKStages * kTile;
-  static constexpr int kOffBar = kOffV + kVStages * kTile;
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2;
+  static constexpr int kOffRing = kOffQ + 2 * kTile;
+  static constexpr int kOffBar = kOffRing + kSlots * kTile;
+  static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -80,6 +80,12 @@ __device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, volatil
   if (!ok) record(site, kDevTimeout);
   return ok;
 }
+
+// Ring order of the K/V tiles of a unit with n key tiles: K_0, then K_m,
+// V_{m-1} for m = 1 .. n-1, then V_{n-1}; MMA step j uses K_j and V_{j-1} and
+// releases both, so slots are released in ring order.
+__device__ __forceinline__ int k_item(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int v_item(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
 struct TileInfo {
   int hq;    // query head
@@ -167,18 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
                        float scale_log2, int pair_heads, int units_per_bh) {
   using L = Layout<D>;
-  constexpr int KS = L::kKStages;
-  constexpr int VS = L::kVStages;
+  constexpr int NS = L::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* bar_q = bars;
-  uint64_t* bar_kfull = bars + 1;
-  uint64_t* bar_kempty = bar_kfull + KS;
-  uint64_t* bar_vfull = bar_kempty + KS;
-  uint64_t* bar_vempty = bar_vfull + VS;
-  uint64_t* bar_sfull = bar_vempty + VS;  // [2]
+  uint64_t* bar_full = bars + 1;          // [NS] ring slot loaded
+  uint64_t* bar_empty = bar_full + NS;    // [NS] ring slot released
+  uint64_t* bar_sfull = bar_empty + NS;   // [2]
   uint64_t* bar_pfull = bar_sfull + 2;    // [2]
   uint64_t* bar_odone = bar_pfull + 2;    // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
@@ -215,17 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < KS; ++s) {
-      mbar_init(bar_kfull + s, 1);
-      mbar_init(bar_kempty + s, 1);
-    }
-    for (int s = 0; s < VS; ++s) {
-      mbar_init(bar_vfull + s, 1);
-      mbar_init(bar_vempty + s, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_full + s, 1);
+      mbar_init(bar_empty + s, 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_sfull + t, 1);
-      mbar_init(bar_pfull + t, 128);
+      mbar_init(bar_pfull + t, 4);  // one arrival per softmax warp
       mbar_init(bar_odone + t, 1);
     }
     *abort_flag = 0;
@@ -241,8 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   uint8_t* sQ = smem + L::kOffQ;
-  uint8_t* sK = smem + L::kOffK;
-  uint8_t* sV = smem + L::kOffV;
+  uint8_t* sRing = smem + L::kOffRing;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -254,22 +252,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t)
         for (int h = 0; h < D / 64; ++h)
           tma_load_4d(sQ + t * L::kTile + h * L::kHalf, &tm_q, bar_q, h * 64, ti[t].hq, ti[t].row0, b);
-      // K_j is consumed at MMA step j, V_{j-1} at step j: load in that order
-      for (int j = 0; j <= n_kt; ++j) {
-        if (j < n_kt) {
-          const int s = j % KS;
-          if (j >= KS && !wait_one(bar_kempty + s, ((j / KS) - 1) & 1, abort_flag, 1)) break;
-          mbar_arrive_expect_tx(bar_kfull + s, L::kTile);
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_kfull + s, h * 64, hkv, j * BN, b);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % VS;
-          if (jj >= VS && !wait_one(bar_vempty + s, ((jj / VS) - 1) & 1, abort_flag, 2)) break;
-          mbar_arrive_expect_tx(bar_vfull + s, L::kTile);
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_vfull + s, h * 64, hkv, jj * BN, b);
-        }
+      for (int item = 0; item < 2 * n_kt; ++item) {
+        const int slot = item % NS;
+        if (item >= NS && !wait_one(bar_empty + slot, ((item / NS) - 1) & 1, abort_flag, 1)) break;
+        // item -> (K or V, key tile), the inverse of k_item / v_item
+        const bool is_v = (item == 2 * n_kt - 1) || (item > 0 && (item & 1) == 0);
+        const int kt = (item == 2 * n_kt - 1) ? n_kt - 1 : (is_v ? item / 2 - 1 : (item + 1) / 2);
+        mbar_arrive_expect_tx(bar_full + slot, L::kTile);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, bar_full + slot, h * 64, hkv,
+                      kt * BN, b);
       }
     }
   } else if (warp == 1) {
@@ -277,12 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kt > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = wait_one(bar_q, 0, abort_flag, 3);
+      // Descriptors are built once; an offset of X bytes is X >> 4 added to
+      // the start-address field (no carry: shared addresses stay below 2^18).
+      const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);          // Q_t, K tiles: K-major
+      const uint64_t dK = sdesc_sw128(smem_u32(sRing), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sRing), L::kHalf, 1024);  // V tiles: MN-major
+      bool ok = wait_one(bar_q, 0, abort_flag, 3) && wait_one(bar_full, 0, abort_flag, 4);  // Q, K_0
       for (int j = 0; ok && j <= n_kt; ++j) {
-        const int ks = j % KS, vs = (j - 1 + VS) % VS;
-        if (j < n_kt && !wait_one(bar_kfull + ks, (j / KS) & 1, abort_flag, 4)) { ok = false; break; }
-        if (j >= 1 && !wait_one(bar_vfull + vs, ((j - 1) / VS) & 1, abort_flag, 5)) { ok = false; break; }
+        const int ki = k_item(j), vi = j >= 1 ? v_item(j - 1, n_kt) : 0;
+        const int ks = ki % NS, vs = vi % NS;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -292,27 +287,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O_t += P_t V_{j-1}; P_t sits in the first 64 columns of S_t
             if (!wait_one(bar_pfull + t, (j - 1) & 1, abort_flag, 6)) { ok = false; break; }
             tc_fence_after();
+            const uint64_t dv = dV + static_cast<uint64_t>((vs * L::kTile) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t db = sdesc_sw128(aV + vs * L::kTile + kk * 16 * 128, L::kHalf, 1024);
-              mma_bf16_ts(tO, tS + kk * 8, db, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_bf16_ts(tO, tS + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
             if (j == ti[t].n_kt) mma_commit(bar_odone + t);
           }
           if (j < ti[t].n_kt) {
             // S_t = Q_t K_j^T (after the P.V that read P_t: MMAs run in issue order)
+            const uint64_t da = dQ + static_cast<uint64_t>((t * L::kTile) >> 4);
+            const uint64_t db = dK + static_cast<uint64_t>((ks * L::kTile) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint64_t da = sdesc_sw128(aQ + t * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
-              const uint64_t db = sdesc_sw128(aK + ks * L::kTile + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
-              mma_bf16_ss(tS, da, db, idesc_qk, kk > 0 ? 1u : 0u);
+              const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
+              mma_bf16_ss(tS, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit(bar_sfull + t);
           }
+          if (t == 0) {
+            // the operands of step j+1 (K_{j+1}, V_j), awaited while the tensor
+            // core still has this step's tile-0 MMAs queued
+            if (j + 1 < n_kt) {
+              const int kn = k_item(j + 1);
+              if (!wait_one(bar_full + kn % NS, (kn / NS) & 1, abort_flag, 4)) { ok = false; break; }
+            }
+            if (j < n_kt) {
+              const int vn = v_item(j, n_kt);
+              if (!wait_one(bar_full + vn % NS, (vn / NS) & 1, abort_flag, 5)) { ok = false; break; }
+            }
+          }
         }
         if (!ok) break;
-        if (j < n_kt) mma_commit(bar_kempty + ks);
-        if (j >= 1) mma_commit(bar_vempty + vs);
       }
     }
   } else if (warp >= 4) {
@@ -323,6 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const int grow = me.row0 + r;
     const int my_kt = me.n_kt;
+    // The tile with more key tiles (tile 1 on a tie) releases the ring slots:
+    // once its S_j is complete, every MMA issued before its QK^T of step j --
+    // all reads of K_j and of V_{j-1} -- has completed.
+    const bool releaser = (me.n_kt == n_kt) && (t == 1 || ti[1].n_kt < n_kt) && r == 0;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + t * 128 + lane_off;
     const uint32_t tO = tmem + 256 + t * 128 + lane_off;
@@ -335,6 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < my_kt; ++j) {
       if (!wait_all(bar_sfull + t, j & 1, abort_flag, 7)) { ok = false; break; }
       tc_fence_after();
+      if (releaser) {
+        mbar_arrive(bar_empty + k_item(j) % NS);
+        if (j >= 1) mbar_arrive(bar_empty + v_item(j - 1, n_kt) % NS);
+      }
       const int kbase = j * BN;
       const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0);
       int lim = BN;  // columns [lim, BN) of this tile are masked for this row
@@ -375,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_new;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_pfull + t);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pfull + t);
     }
 
     // ---------------------------------------------------------------- epilogue
