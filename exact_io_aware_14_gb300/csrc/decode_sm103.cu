@@ -5,13 +5,13 @@
 //
 // Split kernel: one CTA per (split of `chunk` keys, KV head, block of up to 4
 // query heads of that KV head's group, batch).  K/V tiles of 64 keys stream
-// through a 3-stage TMA ring; each K and V byte is read once per CTA and
+// through a 2-stage TMA ring; each K and V byte is read once per CTA and
 // serves every query head of the group.  Per tile: scores on CUDA cores ->
 // online softmax (running max m, sum l, rescale only when m moved) -> P V
 // accumulation in registers.  The CTA writes its split's normalised partial
 // output and natural-log LSE.  Decode is memory-bound ("FlashAttention:
-// Part 2", section 4.1), so the kernel is built to keep HBM busy: two CTAs
-// per SM, ~64 KB of loads in flight per CTA.
+// Part 2", section 4.1), so the kernel is built to keep HBM busy: three
+// CTAs per SM, up to 64 KB of loads in flight per CTA.
 //
 // Combine kernel: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
 #include <cuda_bf16.h>
@@ -28,7 +28,7 @@ __device__ uint32_t g_decode_status;
 constexpr int KT = 64;        // keys per tile
 constexpr int HPC = 4;        // query heads per CTA
 constexpr int kThreads = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 template <int D>
@@ -53,7 +53,7 @@ __device__ __forceinline__ void record(uint32_t site, uint32_t code) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens, int max_seqlen,
                         int Hq, int Hkv, int chunk, int n_split, float scale_log2, float* __restrict__ o_part,
@@ -133,9 +133,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int NG = L::kNG;          // key groups in the PV phase
   const int dp = tid % NDP;
   const int grp = tid / NDP;
-  float acc[HPC][2];
+  float2 acc[HPC];  // dims (2dp, 2dp+1) of each head
 #pragma unroll
-  for (int h = 0; h < HPC; ++h) acc[h][0] = acc[h][1] = 0.f;
+  for (int h = 0; h < HPC; ++h) acc[h] = make_float2(0.f, 0.f);
 
   const int qk_key = tid % KT;
   const int qk_hp = tid / KT;  // heads 2*qk_hp, 2*qk_hp + 1
@@ -163,25 +163,32 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
 
-    // scores of key qk_key for heads 2*qk_hp and 2*qk_hp+1
+    // scores of key qk_key for heads 2*qk_hp and 2*qk_hp+1 (packed fp32x2 FMAs,
+    // four independent partial sums per head)
     {
-      float d0 = 0.f, d1 = 0.f;
+      float2 a0 = make_float2(0.f, 0.f), a0b = a0, a1 = a0, a1b = a0;
       const float* q0 = sQ + (2 * qk_hp) * D;
       const float* q1 = q0 + D;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 kv = ld_shared_v4(kbase + (c >> 3) * L::kHalf + qk_key * 128 + (((c & 7) ^ (qk_key & 7)) << 4));
-        const float4 a0 = *reinterpret_cast<const float4*>(q0 + 8 * c);
-        const float4 a1 = *reinterpret_cast<const float4*>(q0 + 8 * c + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(q1 + 8 * c);
-        const float4 b1 = *reinterpret_cast<const float4*>(q1 + 8 * c + 4);
-        const float k_0 = bf16lo(kv.x), k_1 = bf16hi(kv.x), k_2 = bf16lo(kv.y), k_3 = bf16hi(kv.y);
-        const float k_4 = bf16lo(kv.z), k_5 = bf16hi(kv.z), k_6 = bf16lo(kv.w), k_7 = bf16hi(kv.w);
-        d0 = fmaf(a0.x, k_0, d0); d0 = fmaf(a0.y, k_1, d0); d0 = fmaf(a0.z, k_2, d0); d0 = fmaf(a0.w, k_3, d0);
-        d0 = fmaf(a1.x, k_4, d0); d0 = fmaf(a1.y, k_5, d0); d0 = fmaf(a1.z, k_6, d0); d0 = fmaf(a1.w, k_7, d0);
-        d1 = fmaf(b0.x, k_0, d1); d1 = fmaf(b0.y, k_1, d1); d1 = fmaf(b0.z, k_2, d1); d1 = fmaf(b0.w, k_3, d1);
-        d1 = fmaf(b1.x, k_4, d1); d1 = fmaf(b1.y, k_5, d1); d1 = fmaf(b1.z, k_6, d1); d1 = fmaf(b1.w, k_7, d1);
+        const float4 x0 = *reinterpret_cast<const float4*>(q0 + 8 * c);
+        const float4 x1 = *reinterpret_cast<const float4*>(q0 + 8 * c + 4);
+        const float4 y0 = *reinterpret_cast<const float4*>(q1 + 8 * c);
+        const float4 y1 = *reinterpret_cast<const float4*>(q1 + 8 * c + 4);
+        const float2 k01 = make_float2(bf16lo(kv.x), bf16hi(kv.x)), k23 = make_float2(bf16lo(kv.y), bf16hi(kv.y));
+        const float2 k45 = make_float2(bf16lo(kv.z), bf16hi(kv.z)), k67 = make_float2(bf16lo(kv.w), bf16hi(kv.w));
+        a0 = ffma2(make_float2(x0.x, x0.y), k01, a0);
+        a0b = ffma2(make_float2(x0.z, x0.w), k23, a0b);
+        a0 = ffma2(make_float2(x1.x, x1.y), k45, a0);
+        a0b = ffma2(make_float2(x1.z, x1.w), k67, a0b);
+        a1 = ffma2(make_float2(y0.x, y0.y), k01, a1);
+        a1b = ffma2(make_float2(y0.z, y0.w), k23, a1b);
+        a1 = ffma2(make_float2(y1.x, y1.y), k45, a1);
+        a1b = ffma2(make_float2(y1.z, y1.w), k67, a1b);
       }
+      const float d0 = (a0.x + a0.y) + (a0b.x + a0b.y);
+      const float d1 = (a1.x + a1.y) + (a1b.x + a1b.y);
       const bool vis = qk_key < valid;
       sS[(2 * qk_hp) * KT + qk_key] = vis ? d0 * scale_log2 : -INFINITY;
       sS[(2 * qk_hp + 1) * KT + qk_key] = vis ? d1 * scale_log2 : -INFINITY;
@@ -213,10 +220,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     {
       const float4 al = *reinterpret_cast<const float4*>(sAlpha);
       if (al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f) {
-        acc[0][0] *= al.x; acc[0][1] *= al.x;
-        acc[1][0] *= al.y; acc[1][1] *= al.y;
-        acc[2][0] *= al.z; acc[2][1] *= al.z;
-        acc[3][0] *= al.w; acc[3][1] *= al.w;
+        acc[0] = fmul2(acc[0], make_float2(al.x, al.x));
+        acc[1] = fmul2(acc[1], make_float2(al.y, al.y));
+        acc[2] = fmul2(acc[2], make_float2(al.z, al.z));
+        acc[3] = fmul2(acc[3], make_float2(al.w, al.w));
       }
       const int col = 2 * dp;
       const uint32_t vcol = vbase + (col >> 6) * L::kHalf;
@@ -228,12 +235,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         asm volatile("ld.shared.b32 %0, [%1];"
                      : "=r"(vv)
                      : "r"(vcol + j * 128 + ((((cbyte >> 4) ^ (j & 7))) << 4) + (cbyte & 15)));
-        const float v0 = bf16lo(vv), v1 = bf16hi(vv);
+        const float2 v = make_float2(bf16lo(vv), bf16hi(vv));
         const float4 p = *reinterpret_cast<const float4*>(sP + j * HPC);
-        acc[0][0] = fmaf(p.x, v0, acc[0][0]); acc[0][1] = fmaf(p.x, v1, acc[0][1]);
-        acc[1][0] = fmaf(p.y, v0, acc[1][0]); acc[1][1] = fmaf(p.y, v1, acc[1][1]);
-        acc[2][0] = fmaf(p.z, v0, acc[2][0]); acc[2][1] = fmaf(p.z, v1, acc[2][1]);
-        acc[3][0] = fmaf(p.w, v0, acc[3][0]); acc[3][1] = fmaf(p.w, v1, acc[3][1]);
+        acc[0] = ffma2(make_float2(p.x, p.x), v, acc[0]);
+        acc[1] = ffma2(make_float2(p.y, p.y), v, acc[1]);
+        acc[2] = ffma2(make_float2(p.z, p.z), v, acc[2]);
+        acc[3] = ffma2(make_float2(p.w, p.w), v, acc[3]);
       }
     }
     __syncthreads();  // stage s, sS and sP are free again
@@ -256,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   // merge the NG key groups, then write the split's normalised output and LSE
 #pragma unroll
   for (int h = 0; h < HPC; ++h) {
-    sRed[(grp * HPC + h) * D + 2 * dp] = acc[h][0];
-    sRed[(grp * HPC + h) * D + 2 * dp + 1] = acc[h][1];
+    sRed[(grp * HPC + h) * D + 2 * dp] = acc[h].x;
+    sRed[(grp * HPC + h) * D + 2 * dp + 1] = acc[h].y;
   }
   if (lane == 0) {
     sM[warp] = m;

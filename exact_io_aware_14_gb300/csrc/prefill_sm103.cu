@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j <= n_kt; ++j) {
         const int ki = k_item(j), vi = j >= 1 ? v_item(j - 1, n_kt) : 0;
         const int ks = ki % NS, vs = vi % NS;
-        tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const uint32_t tS = tmem + t * 128;
