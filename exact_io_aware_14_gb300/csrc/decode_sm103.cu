@@ -3,15 +3,23 @@
 // query the cache is split across thread blocks and the partial results are
 // combined).
 //
-// Split kernel: one CTA per (split of `chunk` keys, KV head, block of up to 4
-// query heads of that KV head's group, batch).  K/V tiles of 64 keys stream
-// through a 2-stage TMA ring; each K and V byte is read once per CTA and
-// serves every query head of the group.  Per tile: scores on CUDA cores ->
-// online softmax (running max m, sum l, rescale only when m moved) -> P V
-// accumulation in registers.  The CTA writes its split's normalised partial
-// output and natural-log LSE.  Decode is memory-bound ("FlashAttention:
-// Part 2", section 4.1), so the kernel is built to keep HBM busy: three
-// CTAs per SM, up to 64 KB of loads in flight per CTA.
+// Split kernel: one CTA (8 warps) per (split of `chunk` keys, KV head, block
+// of up to 4 query heads of that KV head's group, batch).  K/V tiles of 64
+// keys stream through a 3-stage TMA ring; each K and V byte is read once per
+// CTA and serves every query head of the block.  Per tile:
+//   scores   8 threads per key, each owning 16 of the 128 head dims for all 4
+//            query heads (q held in registers), packed fp32x2 FMAs, then a
+//            3-level shuffle reduction across the 8 threads;
+//   softmax  one warp per head: tile max, exponent reference moved only when
+//            the max rises by more than 2^8 (same rule as the prefill
+//            kernel), p = 2^(s*c - m*c), running sum;
+//   P V      each thread owns 2 output dims of the 4 heads for a quarter of
+//            the keys, packed fp32x2 FMAs.
+// Two block barriers per tile; the next TMA refill is issued right after the
+// first one, which already proves the previous tile's stage is free.  The CTA
+// writes its split's normalised partial output and natural-log LSE.  Decode is
+// memory-bound ("FlashAttention: Part 2", section 4.1): the kernel exists to
+// keep ~128 KB of loads in flight per SM with few instructions per byte.
 //
 // Combine kernel: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
 #include <cuda_bf16.h>
@@ -27,9 +35,10 @@ __device__ uint32_t g_decode_status;
 
 constexpr int KT = 64;        // keys per tile
 constexpr int HPC = 4;        // query heads per CTA
-constexpr int kThreads = 128;
-constexpr int kStages = 2;
+constexpr int kThreads = 256;
+constexpr int kStages = 3;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kRescaleLog2 = 8.f;  // see the prefill kernel
 
 template <int D>
 struct DLayout {
@@ -37,13 +46,13 @@ struct DLayout {
   static constexpr int kTile = KT * D * 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kTile;
-  static constexpr int kOffQ = kOffV + kStages * kTile;        // float [HPC][D]
-  static constexpr int kOffS = kOffQ + HPC * D * 4;            // float [HPC][KT]
-  static constexpr int kOffP = kOffS + HPC * KT * 4;           // float [KT][HPC]
-  static constexpr int kNG = kThreads / (D / 2);               // key groups in the PV phase
-  static constexpr int kOffRed = kOffP + KT * HPC * 4;         // float [kNG][HPC][D]
-  static constexpr int kOffA = kOffRed + kNG * HPC * D * 4;    // float alpha[HPC], m[HPC], l[HPC]
-  static constexpr int kOffBar = kOffA + 3 * HPC * 4 + 16;
+  static constexpr int kOffS = kOffV + kStages * kTile;        // float [2][HPC][KT] (double-buffered)
+  static constexpr int kOffP = kOffS + 2 * HPC * KT * 4;       // float [2][KT][HPC]
+  static constexpr int kOffA = kOffP + 2 * KT * HPC * 4;       // float [2][HPC] alpha
+  static constexpr int kNG = kThreads / (D / 2);               // key groups in the P.V phase
+  static constexpr int kOffRed = kOffA + 2 * HPC * 4;          // float [kNG][HPC][D]
+  static constexpr int kOffML = kOffRed + kNG * HPC * D * 4;   // float m[HPC], l[HPC]
+  static constexpr int kOffBar = kOffML + 2 * HPC * 4 + 16;
   static constexpr int kBytes = kOffBar + kStages * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -53,12 +62,13 @@ __device__ __forceinline__ void record(uint32_t site, uint32_t code) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens, int max_seqlen,
                         int Hq, int Hkv, int chunk, int n_split, float scale_log2, float* __restrict__ o_part,
                         float* __restrict__ lse_part) {
   using L = DLayout<D>;
+  constexpr int NCH = D / 64;  // 16-byte chunks per key that one score thread reads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -83,25 +93,36 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int hq0 = hkv * G + hb * HPC;
   const int nh = min(HPC, G - hb * HPC);
 
-  float* sQ = reinterpret_cast<float*>(smem + L::kOffQ);
   float* sS = reinterpret_cast<float*>(smem + L::kOffS);
   float* sP = reinterpret_cast<float*>(smem + L::kOffP);
-  float* sRed = reinterpret_cast<float*>(smem + L::kOffRed);
   float* sAlpha = reinterpret_cast<float*>(smem + L::kOffA);
-  float* sM = sAlpha + HPC;
+  float* sRed = reinterpret_cast<float*>(smem + L::kOffRed);
+  float* sM = reinterpret_cast<float*>(smem + L::kOffML);
   float* sL = sM + HPC;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffA + 3 * HPC * 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffML + 2 * HPC * 4);
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
 
-  // query heads of this CTA -> fp32 in shared memory (missing heads read as 0)
-  for (int idx = tid; idx < HPC * D; idx += kThreads) {
-    const int h = idx / D, dd = idx % D;
-    float x = 0.f;
-    if (h < nh) x = __bfloat162float(q[(static_cast<size_t>(b) * Hq + hq0 + h) * D + dd]);
-    sQ[idx] = x;
+  // score role: key slot ks (keys ks and ks + 32 of each tile), dim segment
+  // dseg: 16-byte chunk dseg of each 64-column half of the key row
+  const int ks = tid >> 3;
+  const int dseg = tid & 7;
+  float qf[HPC][NCH * 8];  // this thread's dims of the 4 query heads (0 for missing heads)
+#pragma unroll
+  for (int h = 0; h < HPC; ++h) {
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (h < nh)
+        raw = *reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq0 + h) * D + 64 * c + 8 * dseg);
+      qf[h][8 * c + 0] = bf16lo(raw.x); qf[h][8 * c + 1] = bf16hi(raw.x);
+      qf[h][8 * c + 2] = bf16lo(raw.y); qf[h][8 * c + 3] = bf16hi(raw.y);
+      qf[h][8 * c + 4] = bf16lo(raw.z); qf[h][8 * c + 5] = bf16hi(raw.z);
+      qf[h][8 * c + 6] = bf16lo(raw.w); qf[h][8 * c + 7] = bf16hi(raw.w);
+    }
   }
+
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar_full + s, 1);
     *abort_flag = 0;
@@ -127,98 +148,118 @@ __global__ void __launch_bounds__(kThreads, 3)
     n_issued = min(n_t, kStages);
   }
 
-  // running state of head `warp` (every lane of that warp holds it)
+  const bool negate = scale_log2 < 0.f;
+  const float c = negate ? -scale_log2 : scale_log2;
+  // running state of head `warp` (warps 0..3; every lane of the warp holds it)
   float m = -INFINITY, l = 0.f;
-  constexpr int NDP = D / 2;          // dimension pairs
-  constexpr int NG = L::kNG;          // key groups in the PV phase
+  constexpr int NDP = D / 2;   // dimension pairs
+  constexpr int NG = L::kNG;   // key groups in the P.V phase
   const int dp = tid % NDP;
   const int grp = tid / NDP;
   float2 acc[HPC];  // dims (2dp, 2dp+1) of each head
 #pragma unroll
   for (int h = 0; h < HPC; ++h) acc[h] = make_float2(0.f, 0.f);
 
-  const int qk_key = tid % KT;
-  const int qk_hp = tid / KT;  // heads 2*qk_hp, 2*qk_hp + 1
   bool ok = true;
-
   int t_stop = n_t;
   for (int t = 0; t < n_t; ++t) {
     const int s = t % kStages;
+    const int buf = t & 1;
     bool got = mbar_wait(bar_full + s, (t / kStages) & 1, abort_flag, kWaitLimitNs);
-    if (!__syncthreads_and(got)) {
+    if (!got) *abort_flag = 1;
+    const int valid = min(KT, kn - t * KT);
+    const uint32_t kbase = smem_u32(sK + s * L::kTile);
+    const uint32_t vbase = smem_u32(sV + s * L::kTile);
+
+    // ---- scores: keys ks and ks+32, this thread's 16 (or 8) dims, 4 heads
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int key = ks + 32 * kk;
+      float2 a[HPC];
+#pragma unroll
+      for (int h = 0; h < HPC; ++h) a[h] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const uint4 kv = ld_shared_v4(kbase + cc * L::kHalf + key * 128 + ((dseg ^ (key & 7)) << 4));
+        const float2 k01 = make_float2(bf16lo(kv.x), bf16hi(kv.x)), k23 = make_float2(bf16lo(kv.y), bf16hi(kv.y));
+        const float2 k45 = make_float2(bf16lo(kv.z), bf16hi(kv.z)), k67 = make_float2(bf16lo(kv.w), bf16hi(kv.w));
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) {
+          a[h] = ffma2(make_float2(qf[h][8 * cc + 0], qf[h][8 * cc + 1]), k01, a[h]);
+          a[h] = ffma2(make_float2(qf[h][8 * cc + 2], qf[h][8 * cc + 3]), k23, a[h]);
+          a[h] = ffma2(make_float2(qf[h][8 * cc + 4], qf[h][8 * cc + 5]), k45, a[h]);
+          a[h] = ffma2(make_float2(qf[h][8 * cc + 6], qf[h][8 * cc + 7]), k67, a[h]);
+        }
+      }
+      float v[HPC];
+#pragma unroll
+      for (int h = 0; h < HPC; ++h) v[h] = a[h].x + a[h].y;
+      // reduce the 4 head sums over the 8 threads of this key: after the
+      // first two levels lane bit 2 selects heads {0,1}/{2,3} and bit 1 the head
+      {
+        const bool hi2 = dseg & 4;
+        const float s0 = hi2 ? v[0] : v[2], s1 = hi2 ? v[1] : v[3];
+        const float r0 = __shfl_xor_sync(0xffffffffu, s0, 4), r1 = __shfl_xor_sync(0xffffffffu, s1, 4);
+        float w0 = (hi2 ? v[2] : v[0]) + r0, w1 = (hi2 ? v[3] : v[1]) + r1;
+        const bool hi1 = dseg & 2;
+        const float s2 = hi1 ? w0 : w1;
+        const float r2 = __shfl_xor_sync(0xffffffffu, s2, 2);
+        float w = (hi1 ? w1 : w0) + r2;
+        w += __shfl_xor_sync(0xffffffffu, w, 1);
+        const int head = ((dseg >> 2) & 1) * 2 + ((dseg >> 1) & 1);
+        if ((dseg & 1) == 0) {
+          float sc = negate ? -w : w;
+          sS[(buf * HPC + head) * KT + key] = (key < valid) ? sc : -INFINITY;
+        }
+      }
+    }
+    __syncthreads();
+    if (*abort_flag) {
       if (tid == 0) record(2, kDevTimeout);
       ok = false;
       t_stop = t;
       break;
     }
-    const int valid = min(KT, kn - t * KT);
-    const uint32_t kbase = smem_u32(sK + s * L::kTile);
-    const uint32_t vbase = smem_u32(sV + s * L::kTile);
-    if (valid < KT) {
-      // rows past the cache length may hold anything (NaN): zero them in V so
-      // that p = 0 contributes exactly nothing
-      for (int idx = tid; idx < (KT - valid) * (D / 8); idx += kThreads) {
-        const int row = valid + idx / (D / 8), c = idx % (D / 8);
-        st_shared_v4(vbase + (c >> 3) * L::kHalf + row * 128 + (((c & 7) ^ (row & 7)) << 4), 0u, 0u, 0u, 0u);
-      }
+    // every thread finished the P.V of tile t-1: its stage can be refilled
+    if (tid == 0 && t >= 1 && t - 1 + kStages < n_t) {
+      issue(t - 1 + kStages);
+      n_issued = t + kStages;
     }
 
-    // scores of key qk_key for heads 2*qk_hp and 2*qk_hp+1 (packed fp32x2 FMAs,
-    // four independent partial sums per head)
-    {
-      float2 a0 = make_float2(0.f, 0.f), a0b = a0, a1 = a0, a1b = a0;
-      const float* q0 = sQ + (2 * qk_hp) * D;
-      const float* q1 = q0 + D;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 kv = ld_shared_v4(kbase + (c >> 3) * L::kHalf + qk_key * 128 + (((c & 7) ^ (qk_key & 7)) << 4));
-        const float4 x0 = *reinterpret_cast<const float4*>(q0 + 8 * c);
-        const float4 x1 = *reinterpret_cast<const float4*>(q0 + 8 * c + 4);
-        const float4 y0 = *reinterpret_cast<const float4*>(q1 + 8 * c);
-        const float4 y1 = *reinterpret_cast<const float4*>(q1 + 8 * c + 4);
-        const float2 k01 = make_float2(bf16lo(kv.x), bf16hi(kv.x)), k23 = make_float2(bf16lo(kv.y), bf16hi(kv.y));
-        const float2 k45 = make_float2(bf16lo(kv.z), bf16hi(kv.z)), k67 = make_float2(bf16lo(kv.w), bf16hi(kv.w));
-        a0 = ffma2(make_float2(x0.x, x0.y), k01, a0);
-        a0b = ffma2(make_float2(x0.z, x0.w), k23, a0b);
-        a0 = ffma2(make_float2(x1.x, x1.y), k45, a0);
-        a0b = ffma2(make_float2(x1.z, x1.w), k67, a0b);
-        a1 = ffma2(make_float2(y0.x, y0.y), k01, a1);
-        a1b = ffma2(make_float2(y0.z, y0.w), k23, a1b);
-        a1 = ffma2(make_float2(y1.x, y1.y), k45, a1);
-        a1b = ffma2(make_float2(y1.z, y1.w), k67, a1b);
-      }
-      const float d0 = (a0.x + a0.y) + (a0b.x + a0b.y);
-      const float d1 = (a1.x + a1.y) + (a1b.x + a1b.y);
-      const bool vis = qk_key < valid;
-      sS[(2 * qk_hp) * KT + qk_key] = vis ? d0 * scale_log2 : -INFINITY;
-      sS[(2 * qk_hp + 1) * KT + qk_key] = vis ? d1 * scale_log2 : -INFINITY;
-    }
-    __syncthreads();
-
-    // online softmax of head `warp` over this tile's 64 scores
-    {
-      const float x0 = sS[warp * KT + lane], x1 = sS[warp * KT + lane + 32];
+    if (warp < HPC) {
+      // ---- online softmax of head `warp` over this tile's 64 scores
+      const float x0 = sS[(buf * HPC + warp) * KT + lane], x1 = sS[(buf * HPC + warp) * KT + lane + 32];
       float mt = fmaxf(x0, x1);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-      const float m_new = fmaxf(m, mt);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float p0 = ex2_approx(x0 - m_use), p1 = ex2_approx(x1 - m_use);
+      const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
+      const float m_new = need ? fmaxf(m, mt) : m;
+      const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
+      float p0 = ex2_approx(fmaf(x0, c, -mc)), p1 = ex2_approx(fmaf(x1, c, -mc));
+      p0 = (lane < valid) ? p0 : 0.f;  // also right for c == 0
+      p1 = (lane + 32 < valid) ? p1 : 0.f;
       float ps = p0 + p1;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-      const float alpha = (m_new == m) ? 1.f : ex2_approx(m - m_use);
+      const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
       l = l * alpha + ps;
       m = m_new;
-      sP[lane * HPC + warp] = p0;
-      sP[(lane + 32) * HPC + warp] = p1;
-      if (lane == 0) sAlpha[warp] = alpha;
+      sP[(buf * KT + lane) * HPC + warp] = p0;
+      sP[(buf * KT + lane + 32) * HPC + warp] = p1;
+      if (lane == 0) sAlpha[buf * HPC + warp] = alpha;
+    } else if (valid < KT) {
+      // rows past the cache length may hold anything (NaN): zero them in V so
+      // that p = 0 contributes exactly nothing
+      for (int idx = tid - 32 * HPC; idx < (KT - valid) * (D / 8); idx += kThreads - 32 * HPC) {
+        const int row = valid + idx / (D / 8), cc = idx % (D / 8);
+        st_shared_v4(vbase + (cc >> 3) * L::kHalf + row * 128 + (((cc & 7) ^ (row & 7)) << 4), 0u, 0u, 0u, 0u);
+      }
     }
     __syncthreads();
 
-    // O += P V for dims (2dp, 2dp+1), keys grp, grp+NG, ...
+    // ---- O += P V for dims (2dp, 2dp+1), keys grp, grp+NG, ...
     {
-      const float4 al = *reinterpret_cast<const float4*>(sAlpha);
+      const float4 al = *reinterpret_cast<const float4*>(sAlpha + buf * HPC);
       if (al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f) {
         acc[0] = fmul2(acc[0], make_float2(al.x, al.x));
         acc[1] = fmul2(acc[1], make_float2(al.y, al.y));
@@ -228,25 +269,20 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int col = 2 * dp;
       const uint32_t vcol = vbase + (col >> 6) * L::kHalf;
       const int cbyte = (col & 63) * 2;
-#pragma unroll 8
+#pragma unroll
       for (int jj = 0; jj < KT / NG; ++jj) {
         const int j = jj * NG + grp;
         uint32_t vv;
         asm volatile("ld.shared.b32 %0, [%1];"
                      : "=r"(vv)
                      : "r"(vcol + j * 128 + ((((cbyte >> 4) ^ (j & 7))) << 4) + (cbyte & 15)));
-        const float2 v = make_float2(bf16lo(vv), bf16hi(vv));
-        const float4 p = *reinterpret_cast<const float4*>(sP + j * HPC);
-        acc[0] = ffma2(make_float2(p.x, p.x), v, acc[0]);
-        acc[1] = ffma2(make_float2(p.y, p.y), v, acc[1]);
-        acc[2] = ffma2(make_float2(p.z, p.z), v, acc[2]);
-        acc[3] = ffma2(make_float2(p.w, p.w), v, acc[3]);
+        const float2 vf = make_float2(bf16lo(vv), bf16hi(vv));
+        const float4 p = *reinterpret_cast<const float4*>(sP + (buf * KT + j) * HPC);
+        acc[0] = ffma2(make_float2(p.x, p.x), vf, acc[0]);
+        acc[1] = ffma2(make_float2(p.y, p.y), vf, acc[1]);
+        acc[2] = ffma2(make_float2(p.z, p.z), vf, acc[2]);
+        acc[3] = ffma2(make_float2(p.w, p.w), vf, acc[3]);
       }
-    }
-    __syncthreads();  // stage s, sS and sP are free again
-    if (tid == 0 && t + kStages < n_t) {
-      issue(t + kStages);
-      n_issued = t + kStages + 1;
     }
   }
 
@@ -261,12 +297,13 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 
   // merge the NG key groups, then write the split's normalised output and LSE
+  __syncthreads();
 #pragma unroll
   for (int h = 0; h < HPC; ++h) {
     sRed[(grp * HPC + h) * D + 2 * dp] = acc[h].x;
     sRed[(grp * HPC + h) * D + 2 * dp + 1] = acc[h].y;
   }
-  if (lane == 0) {
+  if (warp < HPC && lane == 0) {
     sM[warp] = m;
     sL[warp] = l;
   }
@@ -279,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     const float lh = sL[h];
     const size_t row = (static_cast<size_t>(b) * Hq + hq0 + h) * n_split + split;
     o_part[row * D + dd] = sum / lh;
-    if (dd == 0) lse_part[row] = (sM[h] + __log2f(lh)) * 0.6931471805599453f;
+    if (dd == 0) lse_part[row] = (sM[h] * c + __log2f(lh)) * 0.6931471805599453f;
   }
 }
 
