@@ -6,22 +6,24 @@
 // Split kernel: one CTA (8 warps) per (split of `chunk` keys, KV head, block
 // of up to 4 query heads of that KV head's group, batch).  K/V tiles of 64
 // keys stream through a 3-stage TMA ring; each K and V byte is read once per
-// CTA and serves every query head of the block.  Per tile:
-//   scores   8 threads per key, each owning 16 of the 128 head dims for all 4
-//            query heads (q held in registers), packed fp32x2 FMAs, then a
-//            3-level shuffle reduction across the 8 threads;
-//   softmax  one warp per head: tile max, exponent reference moved only when
-//            the max rises by more than 2^8 (same rule as the prefill
-//            kernel), p = 2^(s*c - m*c), running sum;
-//   P V      each thread owns 2 output dims of the 4 heads for a quarter of
-//            the keys, packed fp32x2 FMAs.
-// Two block barriers per tile; the next TMA refill is issued right after the
-// first one, which already proves the previous tile's stage is free.  The CTA
-// writes its split's normalised partial output and natural-log LSE.  Decode is
-// memory-bound ("FlashAttention: Part 2", section 4.1): the kernel exists to
-// keep ~128 KB of loads in flight per SM with few instructions per byte.
+// CTA and serves every query head of the block.  The warps are specialised
+// and hand tiles over through mbarriers (no block-wide barrier in the loop),
+// so the scores of tile t+1 overlap the P.V of tile t:
+//   warps 0-3  scores: 8 threads per key, each owning 16 of the 128 head dims
+//              of the 4 query heads (q held in registers), packed fp32x2 FMAs
+//              and a 3-level shuffle reduction; then one warp per head runs
+//              the online softmax (exponent reference moved only when the max
+//              rises by more than 2^8, as in the prefill kernel) and writes
+//              P.  Thread 0 also issues the TMA loads.
+//   warps 4-7  P.V: each thread owns 4 output dims of the 4 heads for a
+//              quarter of the keys, packed fp32x2 FMAs.
+// The CTA writes its split's normalised partial output and natural-log LSE.
+// Decode is memory-bound ("FlashAttention: Part 2", section 4.1): the kernel
+// exists to keep ~128 KB of loads in flight per SM with few instructions per
+// byte.
 //
-// Combine kernel: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
+// Combine kernel: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s;
+// launched as a programmatic dependent of the split kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,6 +38,7 @@ __device__ uint32_t g_decode_status;
 constexpr int KT = 64;        // keys per tile
 constexpr int HPC = 4;        // query heads per CTA
 constexpr int kThreads = 256;
+constexpr int kScoreThreads = 128;  // warps 0-3
 constexpr int kStages = 3;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.f;  // see the prefill kernel
@@ -44,21 +47,42 @@ template <int D>
 struct DLayout {
   static constexpr int kHalf = KT * 128;  // one 64-column box: 64 rows x 128 B
   static constexpr int kTile = KT * D * 2;
+  static constexpr int kDQ = D / 4;                       // 4-dim groups per row (P.V role)
+  static constexpr int kNG = 128 / kDQ;                   // key groups in the P.V role
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kTile;
-  static constexpr int kOffS = kOffV + kStages * kTile;        // float [2][HPC][KT] (double-buffered)
-  static constexpr int kOffP = kOffS + 2 * HPC * KT * 4;       // float [2][KT][HPC]
-  static constexpr int kOffA = kOffP + 2 * KT * HPC * 4;       // float [2][HPC] alpha
-  static constexpr int kNG = kThreads / (D / 2);               // key groups in the P.V phase
-  static constexpr int kOffRed = kOffA + 2 * HPC * 4;          // float [kNG][HPC][D]
-  static constexpr int kOffML = kOffRed + kNG * HPC * D * 4;   // float m[HPC], l[HPC]
-  static constexpr int kOffBar = kOffML + 2 * HPC * 4 + 16;
-  static constexpr int kBytes = kOffBar + kStages * 8 + 16;
+  static constexpr int kOffS = kOffV + kStages * kTile;   // float [2][HPC][KT]
+  static constexpr int kOffP = kOffS + 2 * HPC * KT * 4;  // float [2][KT][HPC]
+  static constexpr int kOffA = kOffP + 2 * KT * HPC * 4;  // float [2][HPC] alpha
+  static constexpr int kOffRed = kOffA + 2 * HPC * 4;     // float [kNG][HPC][D]
+  static constexpr int kOffML = kOffRed + kNG * HPC * D * 4;  // float m[HPC], l[HPC], abort flag
+  static constexpr int kOffBar = kOffML + 2 * HPC * 4 + 16;   // full[kStages], pfull[2], pfree[2]
+  static constexpr int kBytes = kOffBar + (kStages + 4) * 8 + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
 __device__ __forceinline__ void record(uint32_t site, uint32_t code) {
   atomicCAS(&g_decode_status, 0u, (site << 8) | code);
+}
+
+// warp-uniform bounded wait
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  bool ok = mbar_wait(bar, parity, abort_flag, kWaitLimitNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// barrier over the score warps (named barrier 1) that also ORs a flag
+__device__ __forceinline__ bool score_bar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(kScoreThreads)
+      : "memory");
+  return r != 0;
 }
 
 template <int D>
@@ -80,6 +104,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int b = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  // the combine kernel may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   int Lb = seqlens[b];
   if (Lb < 0 || Lb > max_seqlen) {
@@ -101,218 +127,231 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* sL = sM + HPC;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffML + 2 * HPC * 4);
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* bar_pfull = bar_full + kStages;  // [2] P of a tile written (4 score warps)
+  uint64_t* bar_pfree = bar_pfull + 2;       // [2] P.V of a tile done (4 P.V warps)
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
 
-  // score role: key slot ks (keys ks and ks + 32 of each tile), dim segment
-  // dseg: 16-byte chunk dseg of each 64-column half of the key row
-  const int ks = tid >> 3;
-  const int dseg = tid & 7;
-  float qf[HPC][NCH * 8];  // this thread's dims of the 4 query heads (0 for missing heads)
-#pragma unroll
-  for (int h = 0; h < HPC; ++h) {
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-      if (h < nh)
-        raw = *reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq0 + h) * D + 64 * c + 8 * dseg);
-      qf[h][8 * c + 0] = bf16lo(raw.x); qf[h][8 * c + 1] = bf16hi(raw.x);
-      qf[h][8 * c + 2] = bf16lo(raw.y); qf[h][8 * c + 3] = bf16hi(raw.y);
-      qf[h][8 * c + 4] = bf16lo(raw.z); qf[h][8 * c + 5] = bf16hi(raw.z);
-      qf[h][8 * c + 6] = bf16lo(raw.w); qf[h][8 * c + 7] = bf16hi(raw.w);
-    }
-  }
-
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar_full + s, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_pfull + i, 4);
+      mbar_init(bar_pfree + i, 4);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
   __syncthreads();
 
-  auto issue = [&](int t) {
-    const int s = t % kStages;
-    const int key = k0 + t * KT;
-    mbar_arrive_expect_tx(bar_full + s, 2 * L::kTile);
-#pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-      tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_full + s, h * 64, hkv, key, b);
-      tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_full + s, h * 64, hkv, key, b);
-    }
-  };
-  int n_issued = 0;  // meaningful in thread 0 only
-  if (tid == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    for (int t = 0; t < n_t && t < kStages; ++t) issue(t);
-    n_issued = min(n_t, kStages);
-  }
-
   const bool negate = scale_log2 < 0.f;
   const float c = negate ? -scale_log2 : scale_log2;
-  // running state of head `warp` (warps 0..3; every lane of the warp holds it)
-  float m = -INFINITY, l = 0.f;
-  constexpr int NDP = D / 2;   // dimension pairs
-  constexpr int NG = L::kNG;   // key groups in the P.V phase
-  const int dp = tid % NDP;
-  const int grp = tid / NDP;
-  float2 acc[HPC];  // dims (2dp, 2dp+1) of each head
-#pragma unroll
-  for (int h = 0; h < HPC; ++h) acc[h] = make_float2(0.f, 0.f);
 
-  bool ok = true;
-  int t_stop = n_t;
-  for (int t = 0; t < n_t; ++t) {
-    const int s = t % kStages;
-    const int buf = t & 1;
-    bool got = mbar_wait(bar_full + s, (t / kStages) & 1, abort_flag, kWaitLimitNs);
-    if (!got) *abort_flag = 1;
-    const int valid = min(KT, kn - t * KT);
-    const uint32_t kbase = smem_u32(sK + s * L::kTile);
-    const uint32_t vbase = smem_u32(sV + s * L::kTile);
-
-    // ---- scores: keys ks and ks+32, this thread's 16 (or 8) dims, 4 heads
+  if (warp < 4) {
+    // ================================================================ scores + softmax
+    auto issue = [&](int t) {
+      const int s = t % kStages;
+      const int key = k0 + t * KT;
+      mbar_arrive_expect_tx(bar_full + s, 2 * L::kTile);
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const int key = ks + 32 * kk;
-      float2 a[HPC];
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_full + s, h * 64, hkv, key, b);
+        tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_full + s, h * 64, hkv, key, b);
+      }
+    };
+    int n_issued = 0;  // meaningful in thread 0 only
+    if (tid == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int t = 0; t < n_t && t < kStages; ++t) issue(t);
+      n_issued = min(n_t, kStages);
+    }
+    // key slot ks (keys ks, ks+16, ks+32, ks+48), 16-byte chunk dseg of each
+    // 64-column half of the key row
+    const int ks = tid >> 3;
+    const int dseg = tid & 7;
+    float qf[HPC][NCH * 8];  // this thread's dims of the 4 query heads (0 for missing heads)
 #pragma unroll
-      for (int h = 0; h < HPC; ++h) a[h] = make_float2(0.f, 0.f);
+    for (int h = 0; h < HPC; ++h) {
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
-        const uint4 kv = ld_shared_v4(kbase + cc * L::kHalf + key * 128 + ((dseg ^ (key & 7)) << 4));
-        const float2 k01 = make_float2(bf16lo(kv.x), bf16hi(kv.x)), k23 = make_float2(bf16lo(kv.y), bf16hi(kv.y));
-        const float2 k45 = make_float2(bf16lo(kv.z), bf16hi(kv.z)), k67 = make_float2(bf16lo(kv.w), bf16hi(kv.w));
-#pragma unroll
-        for (int h = 0; h < HPC; ++h) {
-          a[h] = ffma2(make_float2(qf[h][8 * cc + 0], qf[h][8 * cc + 1]), k01, a[h]);
-          a[h] = ffma2(make_float2(qf[h][8 * cc + 2], qf[h][8 * cc + 3]), k23, a[h]);
-          a[h] = ffma2(make_float2(qf[h][8 * cc + 4], qf[h][8 * cc + 5]), k45, a[h]);
-          a[h] = ffma2(make_float2(qf[h][8 * cc + 6], qf[h][8 * cc + 7]), k67, a[h]);
-        }
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (h < nh)
+          raw = *reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + hq0 + h) * D + 64 * cc + 8 * dseg);
+        qf[h][8 * cc + 0] = bf16lo(raw.x); qf[h][8 * cc + 1] = bf16hi(raw.x);
+        qf[h][8 * cc + 2] = bf16lo(raw.y); qf[h][8 * cc + 3] = bf16hi(raw.y);
+        qf[h][8 * cc + 4] = bf16lo(raw.z); qf[h][8 * cc + 5] = bf16hi(raw.z);
+        qf[h][8 * cc + 6] = bf16lo(raw.w); qf[h][8 * cc + 7] = bf16hi(raw.w);
       }
-      float v[HPC];
+    }
+    float m = -INFINITY, l = 0.f;  // running state of head `warp`
+    int t_stop = n_t;
+    for (int t = 0; t < n_t; ++t) {
+      const int s = t % kStages;
+      const int buf = t & 1;
+      const bool got = wait_all(bar_full + s, (t / kStages) & 1, abort_flag);
+      const int valid = min(KT, kn - t * KT);
+      const uint32_t kbase = smem_u32(sK + s * L::kTile);
+      const uint32_t vbase = smem_u32(sV + s * L::kTile);
 #pragma unroll
-      for (int h = 0; h < HPC; ++h) v[h] = a[h].x + a[h].y;
-      // reduce the 4 head sums over the 8 threads of this key: after the
-      // first two levels lane bit 2 selects heads {0,1}/{2,3} and bit 1 the head
-      {
+      for (int kk = 0; kk < 4; ++kk) {
+        const int key = ks + 16 * kk;
+        float2 a[HPC];
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) a[h] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int cc = 0; cc < NCH; ++cc) {
+          const uint4 kv = ld_shared_v4(kbase + cc * L::kHalf + key * 128 + ((dseg ^ (key & 7)) << 4));
+          const float2 k01 = make_float2(bf16lo(kv.x), bf16hi(kv.x)), k23 = make_float2(bf16lo(kv.y), bf16hi(kv.y));
+          const float2 k45 = make_float2(bf16lo(kv.z), bf16hi(kv.z)), k67 = make_float2(bf16lo(kv.w), bf16hi(kv.w));
+#pragma unroll
+          for (int h = 0; h < HPC; ++h) {
+            a[h] = ffma2(make_float2(qf[h][8 * cc + 0], qf[h][8 * cc + 1]), k01, a[h]);
+            a[h] = ffma2(make_float2(qf[h][8 * cc + 2], qf[h][8 * cc + 3]), k23, a[h]);
+            a[h] = ffma2(make_float2(qf[h][8 * cc + 4], qf[h][8 * cc + 5]), k45, a[h]);
+            a[h] = ffma2(make_float2(qf[h][8 * cc + 6], qf[h][8 * cc + 7]), k67, a[h]);
+          }
+        }
+        float v[HPC];
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) v[h] = a[h].x + a[h].y;
+        // reduce the 4 head sums over the 8 threads of this key: after the
+        // first two levels lane bit 2 selects heads {0,1}/{2,3} and bit 1 the head
         const bool hi2 = dseg & 4;
         const float s0 = hi2 ? v[0] : v[2], s1 = hi2 ? v[1] : v[3];
         const float r0 = __shfl_xor_sync(0xffffffffu, s0, 4), r1 = __shfl_xor_sync(0xffffffffu, s1, 4);
-        float w0 = (hi2 ? v[2] : v[0]) + r0, w1 = (hi2 ? v[3] : v[1]) + r1;
+        const float w0 = (hi2 ? v[2] : v[0]) + r0, w1 = (hi2 ? v[3] : v[1]) + r1;
         const bool hi1 = dseg & 2;
-        const float s2 = hi1 ? w0 : w1;
-        const float r2 = __shfl_xor_sync(0xffffffffu, s2, 2);
+        const float r2 = __shfl_xor_sync(0xffffffffu, hi1 ? w0 : w1, 2);
         float w = (hi1 ? w1 : w0) + r2;
         w += __shfl_xor_sync(0xffffffffu, w, 1);
-        const int head = ((dseg >> 2) & 1) * 2 + ((dseg >> 1) & 1);
         if ((dseg & 1) == 0) {
-          float sc = negate ? -w : w;
-          sS[(buf * HPC + head) * KT + key] = (key < valid) ? sc : -INFINITY;
+          const int head = ((dseg >> 2) & 1) * 2 + ((dseg >> 1) & 1);
+          sS[(buf * HPC + head) * KT + key] = (key < valid) ? (negate ? -w : w) : -INFINITY;
+        }
+      }
+      // all scores of the tile written; the abort decision is made together
+      if (score_bar_or(!got || *abort_flag)) {
+        if (tid == 0) record(2, kDevTimeout);
+        *abort_flag = 1;
+        t_stop = t;
+        break;
+      }
+      // P buffer `buf` is free once the P.V of tile t-2 is done.  A failed
+      // wait only raises the flag: the score warps leave the loop together at
+      // the next score barrier, so none is left waiting there.
+      if (t >= 2 && !wait_all(bar_pfree + buf, ((t - 2) >> 1) & 1, abort_flag)) {
+        if (lane == 0) record(3, kDevTimeout);
+      }
+      // online softmax of head `warp` over this tile's 64 scores
+      {
+        const float x0 = sS[(buf * HPC + warp) * KT + lane], x1 = sS[(buf * HPC + warp) * KT + lane + 32];
+        float mt = fmaxf(x0, x1);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+        const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
+        const float m_new = need ? fmaxf(m, mt) : m;
+        const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
+        float p0 = ex2_approx(fmaf(x0, c, -mc)), p1 = ex2_approx(fmaf(x1, c, -mc));
+        p0 = (lane < valid) ? p0 : 0.f;  // also right for c == 0
+        p1 = (lane + 32 < valid) ? p1 : 0.f;
+        float ps = p0 + p1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
+        l = l * alpha + ps;
+        m = m_new;
+        sP[(buf * KT + lane) * HPC + warp] = p0;
+        sP[(buf * KT + lane + 32) * HPC + warp] = p1;
+        if (lane == 0) sAlpha[buf * HPC + warp] = alpha;
+      }
+      if (valid < KT) {
+        // rows past the cache length may hold anything (NaN): zero them in V so
+        // that p = 0 contributes exactly nothing
+        for (int idx = tid; idx < (KT - valid) * (D / 8); idx += kScoreThreads) {
+          const int row = valid + idx / (D / 8), cc = idx % (D / 8);
+          st_shared_v4(vbase + (cc >> 3) * L::kHalf + row * 128 + (((cc & 7) ^ (row & 7)) << 4), 0u, 0u, 0u, 0u);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pfull + buf);
+      // refill the stage of tile t-1 once its P.V is done
+      if (warp == 0 && t >= 1 && t - 1 + kStages < n_t) {
+        if (!wait_all(bar_pfree + ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag)) {
+          if (lane == 0) record(4, kDevTimeout);
+        } else if (lane == 0) {
+          issue(t - 1 + kStages);
+          n_issued = t + kStages;
         }
       }
     }
-    __syncthreads();
-    if (*abort_flag) {
-      if (tid == 0) record(2, kDevTimeout);
-      ok = false;
-      t_stop = t;
-      break;
-    }
-    // every thread finished the P.V of tile t-1: its stage can be refilled
-    if (tid == 0 && t >= 1 && t - 1 + kStages < n_t) {
-      issue(t - 1 + kStages);
-      n_issued = t + kStages;
-    }
-
-    if (warp < HPC) {
-      // ---- online softmax of head `warp` over this tile's 64 scores
-      const float x0 = sS[(buf * HPC + warp) * KT + lane], x1 = sS[(buf * HPC + warp) * KT + lane + 32];
-      float mt = fmaxf(x0, x1);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-      const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
-      const float m_new = need ? fmaxf(m, mt) : m;
-      const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
-      float p0 = ex2_approx(fmaf(x0, c, -mc)), p1 = ex2_approx(fmaf(x1, c, -mc));
-      p0 = (lane < valid) ? p0 : 0.f;  // also right for c == 0
-      p1 = (lane + 32 < valid) ? p1 : 0.f;
-      float ps = p0 + p1;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-      const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
-      l = l * alpha + ps;
-      m = m_new;
-      sP[(buf * KT + lane) * HPC + warp] = p0;
-      sP[(buf * KT + lane + 32) * HPC + warp] = p1;
-      if (lane == 0) sAlpha[buf * HPC + warp] = alpha;
-    } else if (valid < KT) {
-      // rows past the cache length may hold anything (NaN): zero them in V so
-      // that p = 0 contributes exactly nothing
-      for (int idx = tid - 32 * HPC; idx < (KT - valid) * (D / 8); idx += kThreads - 32 * HPC) {
-        const int row = valid + idx / (D / 8), cc = idx % (D / 8);
-        st_shared_v4(vbase + (cc >> 3) * L::kHalf + row * 128 + (((cc & 7) ^ (row & 7)) << 4), 0u, 0u, 0u, 0u);
-      }
-    }
-    __syncthreads();
-
-    // ---- O += P V for dims (2dp, 2dp+1), keys grp, grp+NG, ...
-    {
-      const float4 al = *reinterpret_cast<const float4*>(sAlpha + buf * HPC);
-      if (al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f) {
-        acc[0] = fmul2(acc[0], make_float2(al.x, al.x));
-        acc[1] = fmul2(acc[1], make_float2(al.y, al.y));
-        acc[2] = fmul2(acc[2], make_float2(al.z, al.z));
-        acc[3] = fmul2(acc[3], make_float2(al.w, al.w));
-      }
-      const int col = 2 * dp;
-      const uint32_t vcol = vbase + (col >> 6) * L::kHalf;
-      const int cbyte = (col & 63) * 2;
-#pragma unroll
-      for (int jj = 0; jj < KT / NG; ++jj) {
-        const int j = jj * NG + grp;
-        uint32_t vv;
-        asm volatile("ld.shared.b32 %0, [%1];"
-                     : "=r"(vv)
-                     : "r"(vcol + j * 128 + ((((cbyte >> 4) ^ (j & 7))) << 4) + (cbyte & 15)));
-        const float2 vf = make_float2(bf16lo(vv), bf16hi(vv));
-        const float4 p = *reinterpret_cast<const float4*>(sP + (buf * KT + j) * HPC);
-        acc[0] = ffma2(make_float2(p.x, p.x), vf, acc[0]);
-        acc[1] = ffma2(make_float2(p.y, p.y), vf, acc[1]);
-        acc[2] = ffma2(make_float2(p.z, p.z), vf, acc[2]);
-        acc[3] = ffma2(make_float2(p.w, p.w), vf, acc[3]);
-      }
-    }
-  }
-
-  // every issued load must land before the CTA may exit (bounded, not abortable)
-  if (!ok) {
-    if (tid == 0) {
+    if (warp == 0 && lane == 0 && *abort_flag) {
+      // every issued load must land before the CTA may exit (bounded, not abortable)
       volatile int no_abort = 0;
       for (int t = t_stop; t < n_issued; ++t)
         if (!mbar_wait(bar_full + (t % kStages), (t / kStages) & 1, &no_abort, kWaitLimitNs)) break;
     }
-    return;
+    if (lane == 0) {
+      sM[warp] = m;
+      sL[warp] = l;
+    }
+  } else {
+    // ================================================================ P.V
+    const int ptid = tid - kScoreThreads;
+    const int dq = ptid % L::kDQ;  // dims 4dq .. 4dq+3
+    const int grp = ptid / L::kDQ;  // keys grp, grp + kNG, ...
+    const int col = 4 * dq;
+    const int cbyte = (col & 63) * 2;  // byte offset inside a 128-B half row (8-byte aligned)
+    float2 acc[HPC][2];
+#pragma unroll
+    for (int h = 0; h < HPC; ++h) acc[h][0] = acc[h][1] = make_float2(0.f, 0.f);
+    for (int t = 0; t < n_t; ++t) {
+      const int s = t % kStages;
+      const int buf = t & 1;
+      if (!wait_all(bar_pfull + buf, (t >> 1) & 1, abort_flag)) break;
+      const float4 al = *reinterpret_cast<const float4*>(sAlpha + buf * HPC);
+      if (al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f) {
+        const float alv[HPC] = {al.x, al.y, al.z, al.w};
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) {
+          acc[h][0] = fmul2(acc[h][0], make_float2(alv[h], alv[h]));
+          acc[h][1] = fmul2(acc[h][1], make_float2(alv[h], alv[h]));
+        }
+      }
+      const uint32_t vcol = smem_u32(sV + s * L::kTile) + (col >> 6) * L::kHalf + (cbyte & 15);
+#pragma unroll
+      for (int jj = 0; jj < KT / L::kNG; ++jj) {
+        const int j = jj * L::kNG + grp;
+        uint32_t v0, v1;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                     : "=r"(v0), "=r"(v1)
+                     : "r"(vcol + j * 128 + ((((cbyte >> 4) ^ (j & 7))) << 4)));
+        const float2 va = make_float2(bf16lo(v0), bf16hi(v0)), vb = make_float2(bf16lo(v1), bf16hi(v1));
+        const float4 p = *reinterpret_cast<const float4*>(sP + (buf * KT + j) * HPC);
+        const float pv[HPC] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) {
+          acc[h][0] = ffma2(make_float2(pv[h], pv[h]), va, acc[h][0]);
+          acc[h][1] = ffma2(make_float2(pv[h], pv[h]), vb, acc[h][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pfree + buf);
+    }
+#pragma unroll
+    for (int h = 0; h < HPC; ++h) {
+      float* dst = sRed + (grp * HPC + h) * D + col;
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+    }
   }
 
-  // merge the NG key groups, then write the split's normalised output and LSE
   __syncthreads();
-#pragma unroll
-  for (int h = 0; h < HPC; ++h) {
-    sRed[(grp * HPC + h) * D + 2 * dp] = acc[h].x;
-    sRed[(grp * HPC + h) * D + 2 * dp + 1] = acc[h].y;
-  }
-  if (warp < HPC && lane == 0) {
-    sM[warp] = m;
-    sL[warp] = l;
-  }
-  __syncthreads();
+  if (*abort_flag) return;
+  // merge the key groups, then write the split's normalised output and LSE
   for (int idx = tid; idx < nh * D; idx += kThreads) {
     const int h = idx / D, dd = idx % D;
     float sum = 0.f;
 #pragma unroll
-    for (int g = 0; g < NG; ++g) sum += sRed[(g * HPC + h) * D + dd];
+    for (int g = 0; g < L::kNG; ++g) sum += sRed[(g * HPC + h) * D + dd];
     const float lh = sL[h];
     const size_t row = (static_cast<size_t>(b) * Hq + hq0 + h) * n_split + split;
     o_part[row * D + dd] = sum / lh;
@@ -329,6 +368,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
   const int b = blockIdx.x / Hq;
   const int hq = blockIdx.x % Hq;
   const int dd = threadIdx.x;
+  // launched as a programmatic dependent of the split kernel: wait until all
+  // of its partials are written and visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int Lb = seqlens[b];
   Lb = Lb < 0 ? 0 : (Lb > max_seqlen ? max_seqlen : Lb);
   const int ns = (Lb + chunk - 1) / chunk;
@@ -364,10 +406,21 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t stream) {
       p.n_split, p.scale_log2, p.o_part, p.lse_part);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<p.B * p.Hq, D, 0, stream>>>(p.o_part, p.lse_part, p.seqlens, p.max_seqlen, p.Hq,
-                                                         p.chunk, p.n_split, static_cast<__nv_bfloat16*>(p.o),
-                                                         p.lse);
-  return cudaGetLastError();
+  // programmatic dependent launch: the combine grid is set up while the split
+  // grid drains, instead of after it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.B * p.Hq);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, static_cast<const float*>(p.o_part),
+                            static_cast<const float*>(p.lse_part), p.seqlens, p.max_seqlen, p.Hq, p.chunk, p.n_split,
+                            static_cast<__nv_bfloat16*>(p.o), p.lse);
 }
 
 }  // namespace
