@@ -55,7 +55,7 @@ struct Layout {
   static constexpr int kOffQ = 0;  // Q_0, Q_1
   static constexpr int kOffRing = kOffQ + 2 * kTile;
   static constexpr int kOffBar = kOffRing + kSlots * kTile;
-  static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2;
+  static constexpr int kNumBars = 2 * kSlots + 6 * 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -166,58 +166,81 @@ __device__ __forceinline__ float score_tile_exp(uint32_t tS, int lim, float c, f
   return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
+// Work unit U -> (batch, KV head, the two query tiles).  Units are numbered
+// (u_rev, head slot, batch) with u_rev slowest, so causal units come longest
+// first.
+struct Unit {
+  int b, hkv, n_kt;
+  TileInfo ti[2];
+};
+__device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
+                                            int pair_heads, int units_per_bh) {
+  Unit u;
+  const int hslots = pair_heads ? Hq / 2 : Hq;
+  const int bh_count = B * hslots;
+  const int u_rev = U / bh_count;
+  const int bh = U % bh_count;
+  const int unit = causal ? (units_per_bh - 1 - u_rev) : u_rev;
+  u.b = bh / hslots;
+  const int hs = bh % hslots;
+  if (pair_heads) {
+    u.ti[0].hq = 2 * hs;
+    u.ti[1].hq = 2 * hs + 1;
+    u.ti[0].row0 = u.ti[1].row0 = unit * BM;
+  } else {
+    u.ti[0].hq = u.ti[1].hq = hs;
+    u.ti[0].row0 = (2 * unit) * BM;
+    u.ti[1].row0 = (2 * unit + 1) * BM;
+  }
+  u.hkv = u.ti[0].hq / (Hq / Hkv);  // both heads of a pair share the KV head
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int kend = causal ? min(Nk, u.ti[t].row0 + BM) : Nk;
+    u.ti[t].n_kt = (u.ti[t].row0 < Nq) ? (kend + BN - 1) / BN : 0;
+  }
+  u.n_kt = max(u.ti[0].n_kt, u.ti[1].n_kt);
+  return u;
+}
+
+// Unit of round r for this CTA: zig-zag over the CTAs (c, then G-1-c, ...),
+// which balances the longest-first causal units across CTAs.  -1: none.
+__device__ __forceinline__ int unit_of_round(int r, int total_units) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int U = r * G + ((r & 1) ? (G - 1 - c) : c);
+  return U < total_units ? U : -1;
+}
+
+// Persistent: each CTA walks the units of rounds r = 0, 1, ... (unit_of_round).
+// Barrier phases run on across units: per-unit barriers by the unit count
+// `uc`, score / P barriers by the running key-tile count of each query tile,
+// ring slots by the running item count.
 template <int D, bool kNeg>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                        float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
-                       float scale_log2, int pair_heads, int units_per_bh) {
+                       float scale_log2, int pair_heads, int units_per_bh, int total_units) {
   using L = Layout<D>;
   constexpr int NS = L::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-  uint64_t* bar_q = bars;
-  uint64_t* bar_full = bars + 1;          // [NS] ring slot loaded
+  uint64_t* bar_full = bars;              // [NS] ring slot loaded
   uint64_t* bar_empty = bar_full + NS;    // [NS] ring slot released
-  uint64_t* bar_sfull = bar_empty + NS;   // [2]
-  uint64_t* bar_pfull = bar_sfull + 2;    // [2]
-  uint64_t* bar_odone = bar_pfull + 2;    // [2]
+  uint64_t* bar_sfull = bar_empty + NS;   // [2] S_t complete
+  uint64_t* bar_pfull = bar_sfull + 2;    // [2] P_t written (4 softmax warps)
+  uint64_t* bar_odone = bar_pfull + 2;    // [2] last P.V of the unit into O_t complete
+  uint64_t* bar_qfull = bar_odone + 2;    // [2] Q_t loaded
+  uint64_t* bar_qfree = bar_qfull + 2;    // [2] last QK^T of the unit read Q_t
+  uint64_t* bar_ofree = bar_qfree + 2;    // [2] epilogue read O_t out of TMEM (4 softmax warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: (unit index, head slot, batch); longest causal units first
-  const int hslots = pair_heads ? Hq / 2 : Hq;
-  const int bh_count = B * hslots;
-  const int u_rev = blockIdx.x / bh_count;
-  const int bh = blockIdx.x % bh_count;
-  const int unit = causal ? (units_per_bh - 1 - u_rev) : u_rev;
-  const int b = bh / hslots;
-  const int hs = bh % hslots;
-  TileInfo ti[2];
-  if (pair_heads) {
-    ti[0].hq = 2 * hs;
-    ti[1].hq = 2 * hs + 1;
-    ti[0].row0 = ti[1].row0 = unit * BM;
-  } else {
-    ti[0].hq = ti[1].hq = hs;
-    ti[0].row0 = (2 * unit) * BM;
-    ti[1].row0 = (2 * unit + 1) * BM;
-  }
-  const int hkv = ti[0].hq / (Hq / Hkv);  // both heads of a pair share the KV head
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int kend = causal ? min(Nk, ti[t].row0 + BM) : Nk;
-    ti[t].n_kt = (ti[t].row0 < Nq) ? (kend + BN - 1) / BN : 0;
-  }
-  const int n_kt = max(ti[0].n_kt, ti[1].n_kt);
-
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_full + s, 1);
       mbar_init(bar_empty + s, 1);
@@ -226,6 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_sfull + t, 1);
       mbar_init(bar_pfull + t, 4);  // one arrival per softmax warp
       mbar_init(bar_odone + t, 1);
+      mbar_init(bar_qfull + t, 1);
+      mbar_init(bar_qfree + t, 1);
+      mbar_init(bar_ofree + t, 4);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -244,29 +270,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0 && n_kt > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
-      for (int t = 0; t < 2; ++t)
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_4d(sQ + t * L::kTile + h * L::kHalf, &tm_q, bar_q, h * 64, ti[t].hq, ti[t].row0, b);
-      for (int item = 0; item < 2 * n_kt; ++item) {
-        const int slot = item % NS;
-        if (item >= NS && !wait_one(bar_empty + slot, ((item / NS) - 1) & 1, abort_flag, 1)) break;
-        // item -> (K or V, key tile), the inverse of k_item / v_item
-        const bool is_v = (item == 2 * n_kt - 1) || (item > 0 && (item & 1) == 0);
-        const int kt = (item == 2 * n_kt - 1) ? n_kt - 1 : (is_v ? item / 2 - 1 : (item + 1) / 2);
-        mbar_arrive_expect_tx(bar_full + slot, L::kTile);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, bar_full + slot, h * 64, hkv,
-                      kt * BN, b);
+      uint32_t item_base = 0;
+      int uc = 0;
+      bool ok = true;
+      for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
+        const int U = unit_of_round(rnd, total_units);
+        if (U < 0) continue;
+        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, pair_heads, units_per_bh);
+        for (int t = 0; t < 2; ++t) {
+          // Q_t of the previous unit must have been read by its last QK^T
+          if (uc >= 1 && !wait_one(bar_qfree + t, (uc - 1) & 1, abort_flag, 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_qfull + t, L::kTile);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_4d(sQ + t * L::kTile + h * L::kHalf, &tm_q, bar_qfull + t, h * 64, u.ti[t].hq, u.ti[t].row0,
+                        u.b);
+        }
+        for (int item = 0; ok && item < 2 * u.n_kt; ++item) {
+          const uint32_t gi = item_base + item;
+          const int slot = gi % NS;
+          if (gi >= NS && !wait_one(bar_empty + slot, ((gi / NS) - 1) & 1, abort_flag, 2)) { ok = false; break; }
+          // item -> (K or V, key tile), the inverse of k_item / v_item
+          const bool is_v = (item == 2 * u.n_kt - 1) || (item > 0 && (item & 1) == 0);
+          const int kt = (item == 2 * u.n_kt - 1) ? u.n_kt - 1 : (is_v ? item / 2 - 1 : (item + 1) / 2);
+          mbar_arrive_expect_tx(bar_full + slot, L::kTile);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, bar_full + slot, h * 64,
+                        u.hkv, kt * BN, u.b);
+        }
+        item_base += 2 * u.n_kt;
+        ++uc;
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_kt > 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
       // Descriptors are built once; an offset of X bytes is X >> 4 added to
@@ -274,154 +315,203 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);          // Q_t, K tiles: K-major
       const uint64_t dK = sdesc_sw128(smem_u32(sRing), 16, 1024);
       const uint64_t dV = sdesc_sw128(smem_u32(sRing), L::kHalf, 1024);  // V tiles: MN-major
-      bool ok = wait_one(bar_q, 0, abort_flag, 3) && wait_one(bar_full, 0, abort_flag, 4);  // Q, K_0
-      for (int j = 0; ok && j <= n_kt; ++j) {
-        const int ki = k_item(j), vi = j >= 1 ? v_item(j - 1, n_kt) : 0;
-        const int ks = ki % NS, vs = vi % NS;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t tS = tmem + t * 128;
-          const uint32_t tO = tmem + 256 + t * 128;
-          if (j >= 1 && j - 1 < ti[t].n_kt) {
-            // O_t += P_t V_{j-1}; P_t sits in the first 64 columns of S_t
-            if (!wait_one(bar_pfull + t, (j - 1) & 1, abort_flag, 6)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t dv = dV + static_cast<uint64_t>((vs * L::kTile) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_bf16_ts(tO, tS + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            if (j == ti[t].n_kt) mma_commit(bar_odone + t);
+      uint32_t item_base = 0;
+      int kc[2] = {0, 0};  // key tiles done per query tile (score / P barrier phases)
+      int uc = 0;
+      bool ok = true;
+      for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
+        const int U = unit_of_round(rnd, total_units);
+        if (U < 0) continue;
+        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, pair_heads, units_per_bh);
+        const int n_kt = u.n_kt;
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = wait_one(bar_qfull + t, uc & 1, abort_flag, 3);
+          if (ok && u.ti[t].n_kt == 0) {
+            // nothing to compute for this tile: hand its per-unit barriers on
+            if (uc >= 1) ok = wait_one(bar_ofree + t, (uc - 1) & 1, abort_flag, 9);
+            mma_commit(bar_qfree + t);
+            mma_commit(bar_odone + t);
           }
-          if (j < ti[t].n_kt) {
-            // S_t = Q_t K_j^T (after the P.V that read P_t: MMAs run in issue order)
-            const uint64_t da = dQ + static_cast<uint64_t>((t * L::kTile) >> 4);
-            const uint64_t db = dK + static_cast<uint64_t>((ks * L::kTile) >> 4);
+        }
+        if (ok && n_kt > 0) ok = wait_one(bar_full + item_base % NS, (item_base / NS) & 1, abort_flag, 4);  // K_0
+        for (int j = 0; ok && j <= n_kt; ++j) {
+          const uint32_t ki = item_base + k_item(j), vi = item_base + (j >= 1 ? v_item(j - 1, n_kt) : 0);
+          const int ks = ki % NS, vs = vi % NS;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
-              mma_bf16_ss(tS, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int t = 0; t < 2; ++t) {
+            const int n_t = u.ti[t].n_kt;
+            const uint32_t tS = tmem + t * 128;
+            const uint32_t tO = tmem + 256 + t * 128;
+            if (j >= 1 && j - 1 < n_t) {
+              // O_t += P_t V_{j-1}; P_t sits in the first 64 columns of S_t
+              if (!wait_one(bar_pfull + t, (kc[t] + j - 1) & 1, abort_flag, 6)) { ok = false; break; }
+              // the first P.V of a unit overwrites O_t: the previous epilogue must have read it
+              if (j == 1 && uc >= 1 && !wait_one(bar_ofree + t, (uc - 1) & 1, abort_flag, 9)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t dv = dV + static_cast<uint64_t>((vs * L::kTile) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_bf16_ts(tO, tS + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              if (j == n_t) mma_commit(bar_odone + t);
             }
-            mma_commit(bar_sfull + t);
-          }
-          if (t == 0) {
-            // the operands of step j+1 (K_{j+1}, V_j), awaited while the tensor
-            // core still has this step's tile-0 MMAs queued
-            if (j + 1 < n_kt) {
-              const int kn = k_item(j + 1);
-              if (!wait_one(bar_full + kn % NS, (kn / NS) & 1, abort_flag, 4)) { ok = false; break; }
+            if (j < n_t) {
+              // S_t = Q_t K_j^T (after the P.V that read P_t: MMAs run in issue order)
+              const uint64_t da = dQ + static_cast<uint64_t>((t * L::kTile) >> 4);
+              const uint64_t db = dK + static_cast<uint64_t>((ks * L::kTile) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
+                mma_bf16_ss(tS, da + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(bar_sfull + t);
+              if (j == n_t - 1) mma_commit(bar_qfree + t);
             }
-            if (j < n_kt) {
-              const int vn = v_item(j, n_kt);
-              if (!wait_one(bar_full + vn % NS, (vn / NS) & 1, abort_flag, 5)) { ok = false; break; }
+            if (t == 0) {
+              // the operands of step j+1 (K_{j+1}, V_j), awaited while the tensor
+              // core still has this step's tile-0 MMAs queued
+              if (j + 1 < n_kt) {
+                const uint32_t kn = item_base + k_item(j + 1);
+                if (!wait_one(bar_full + kn % NS, (kn / NS) & 1, abort_flag, 4)) { ok = false; break; }
+              }
+              if (j < n_kt) {
+                const uint32_t vn = item_base + v_item(j, n_kt);
+                if (!wait_one(bar_full + vn % NS, (vn / NS) & 1, abort_flag, 5)) { ok = false; break; }
+              }
             }
           }
         }
-        if (!ok) break;
+        kc[0] += u.ti[0].n_kt;
+        kc[1] += u.ti[1].n_kt;
+        item_base += 2 * n_kt;
+        ++uc;
       }
     }
   } else if (warp >= 4) {
-    // ---------------------------------------------------------------- softmax
+    // ---------------------------------------------------------------- softmax + epilogue
     const int t = (warp - 4) >> 2;  // query tile of this warpgroup
-    const TileInfo me = t ? ti[1] : ti[0];
     const int quarter = warp & 3;  // TMEM lanes this warp may touch: 32*quarter .. +31
     const int r = quarter * 32 + lane;
-    const int grow = me.row0 + r;
-    const int my_kt = me.n_kt;
-    // The tile with more key tiles (tile 1 on a tie) releases the ring slots:
-    // once its S_j is complete, every MMA issued before its QK^T of step j --
-    // all reads of K_j and of V_{j-1} -- has completed.
-    const bool releaser = (me.n_kt == n_kt) && (t == 1 || ti[1].n_kt < n_kt) && r == 0;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + t * 128 + lane_off;
     const uint32_t tO = tmem + 256 + t * 128 + lane_off;
     // with a negative scale the kernel works on -s with |c| (kNeg), so the
     // max logic is the same
     const float c = kNeg ? -scale_log2 : scale_log2;
-    float m = -INFINITY;  // exponent reference of this row (sign-adjusted raw score units)
-    float l = 0.f;        // running sum of 2^(s*c - m*c)
+    const bool o_32b_aligned = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+    uint32_t item_base = 0;
+    int kc = 0, uc = 0;
     bool ok = true;
-    for (int j = 0; j < my_kt; ++j) {
-      if (!wait_all(bar_sfull + t, j & 1, abort_flag, 7)) { ok = false; break; }
-      tc_fence_after();
-      if (releaser) {
-        mbar_arrive(bar_empty + k_item(j) % NS);
-        if (j >= 1) mbar_arrive(bar_empty + v_item(j - 1, n_kt) % NS);
-      }
-      const int kbase = j * BN;
-      const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0);
-      int lim = BN;  // columns [lim, BN) of this tile are masked for this row
-      if (masked) {
-        lim = Nk - kbase;
-        if (causal) lim = min(lim, grow - kbase + 1);
-      }
-      const float mt = masked ? score_tile_max<true, kNeg>(tS, lim) : score_tile_max<false, kNeg>(tS, lim);
-      // move the reference only on the first visible scores or when the tile
-      // max is more than 2^kRescaleLog2 above it
-      const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
-      const float m_new = need ? fmaxf(m, mt) : m;
-      const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
-      const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
-      const float rowsum = masked ? score_tile_exp<true, kNeg>(tS, lim, c, mc)
-                                  : score_tile_exp<false, kNeg>(tS, lim, c, mc);
-      l = l * alpha + rowsum;
-
-      // O_t holds the sum through tile j-1 (P.V of j-1 completed before S_j was
-      // written): rescale it now if this row's reference moved.
-      if (j > 0 && __any_sync(0xffffffffu, need && m != -INFINITY)) {
-        const float a = (need && m != -INFINITY) ? alpha : 1.f;
-        const float2 a2 = make_float2(a, a);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t u[32];
-          tmem_ld32(tO + cc * 32, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = fmul2(make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])), a2);
-            u[2 * i] = __float_as_uint(x.x);
-            u[2 * i + 1] = __float_as_uint(x.y);
-          }
-          tmem_st32(tO + cc * 32, u);
+    for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
+      const int U = unit_of_round(rnd, total_units);
+      if (U < 0) continue;
+      const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, pair_heads, units_per_bh);
+      const TileInfo me = t ? u.ti[1] : u.ti[0];
+      const int grow = me.row0 + r;
+      const int my_kt = me.n_kt;
+      // The tile with more key tiles (tile 1 on a tie) releases the ring slots:
+      // once its S_j is complete, every MMA issued before its QK^T of step j --
+      // all reads of K_j and of V_{j-1} -- has completed; V_{n-1} is released
+      // after its last P.V.
+      const bool releaser = (my_kt == u.n_kt) && (t == 1 || u.ti[1].n_kt < u.n_kt) && r == 0 && my_kt > 0;
+      float m = -INFINITY;  // exponent reference of this row (sign-adjusted raw score units)
+      float l = 0.f;        // running sum of 2^(s*c - m*c)
+      for (int j = 0; j < my_kt; ++j) {
+        if (!wait_all(bar_sfull + t, (kc + j) & 1, abort_flag, 7)) { ok = false; break; }
+        tc_fence_after();
+        if (releaser) {
+          mbar_arrive(bar_empty + (item_base + k_item(j)) % NS);
+          if (j >= 1) mbar_arrive(bar_empty + (item_base + v_item(j - 1, u.n_kt)) % NS);
         }
-      }
-      m = m_new;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pfull + t);
-    }
+        const int kbase = j * BN;
+        const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0);
+        int lim = BN;  // columns [lim, BN) of this tile are masked for this row
+        if (masked) {
+          lim = Nk - kbase;
+          if (causal) lim = min(lim, grow - kbase + 1);
+        }
+        const float mt = masked ? score_tile_max<true, kNeg>(tS, lim) : score_tile_max<false, kNeg>(tS, lim);
+        // move the reference only on the first visible scores or when the tile
+        // max is more than 2^kRescaleLog2 above it
+        const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
+        const float m_new = need ? fmaxf(m, mt) : m;
+        const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
+        const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
+        const float rowsum = masked ? score_tile_exp<true, kNeg>(tS, lim, c, mc)
+                                    : score_tile_exp<false, kNeg>(tS, lim, c, mc);
+        l = l * alpha + rowsum;
 
-    // ---------------------------------------------------------------- epilogue
-    if (ok && my_kt > 0) ok = wait_all(bar_odone + t, 0, abort_flag, 8);
-    if (ok && me.row0 < Nq) {
+        // O_t holds the sum through tile j-1 (P.V of j-1 completed before S_j was
+        // written): rescale it now if this row's reference moved.
+        if (j > 0 && __any_sync(0xffffffffu, need && m != -INFINITY)) {
+          const float a = (need && m != -INFINITY) ? alpha : 1.f;
+          const float2 a2 = make_float2(a, a);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t w[32];
+            tmem_ld32(tO + cc * 32, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = fmul2(make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1])), a2);
+              w[2 * i] = __float_as_uint(x.x);
+              w[2 * i + 1] = __float_as_uint(x.y);
+            }
+            tmem_st32(tO + cc * 32, w);
+          }
+        }
+        m = m_new;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pfull + t);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------------- epilogue
+      if (!wait_all(bar_odone + t, uc & 1, abort_flag, 8)) { ok = false; break; }
       tc_fence_after();
-      const bool store = grow < Nq;
-      __nv_bfloat16* orow = out + ((static_cast<size_t>(b) * Nq + grow) * Hq + me.hq) * D;
+      if (releaser) mbar_arrive(bar_empty + (item_base + 2 * u.n_kt - 1) % NS);  // V_{n-1}
+      const bool store = me.row0 < Nq && grow < Nq;
+      __nv_bfloat16* orow = out + ((static_cast<size_t>(u.b) * Nq + grow) * Hq + me.hq) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t u[32];
+        uint32_t w32[32];
         if (my_kt > 0) {
-          tmem_ld32(tO + cc * 32, u);
+          tmem_ld32(tO + cc * 32, w32);
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = 0u;
+          for (int i = 0; i < 32; ++i) w32[i] = 0u;
+        }
+        if (cc == D / 32 - 1) {
+          // O_t has been read out of TMEM: the next unit's first P.V may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_ofree + t);
         }
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l, __uint_as_float(u[2 * i + 1]) * inv_l);
+          w[i] = pack_bf16x2(__uint_as_float(w32[2 * i]) * inv_l, __uint_as_float(w32[2 * i + 1]) * inv_l);
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+          if (o_32b_aligned) {  // 32-byte stores: a warp writes 32 full sectors per instruction
+            st_global_v8(orow + cc * 32, w);
+            st_global_v8(orow + cc * 32 + 16, w + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
       }
       if (store) {
         const float lse = (l > 0.f) ? (m * c + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-        lse_out[(static_cast<size_t>(b) * Hq + me.hq) * Nq + grow] = lse;
+        lse_out[(static_cast<size_t>(u.b) * Hq + me.hq) * Nq + grow] = lse;
       }
+      kc += my_kt;
+      item_base += 2 * u.n_kt;
+      ++uc;
     }
   }
 
@@ -442,15 +532,20 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
   const int pair_heads = (G % 2 == 0) ? 1 : 0;
   const int units_per_bh = pair_heads ? n_qtiles : (n_qtiles + 1) / 2;
   const int hslots = pair_heads ? p.Hq / 2 : p.Hq;
-  const long long blocks = static_cast<long long>(units_per_bh) * p.B * hslots;
-  if (blocks == 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto kern = (p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true> : prefill_fwd_kernel<D, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  const long long total = static_cast<long long>(units_per_bh) * p.B * hslots;
+  if (total == 0) return cudaSuccess;
+  if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  int dev = 0, n_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(blocks), kThreads, L::kAlloc, stream>>>(
-      p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.causal,
-      p.scale_log2, pair_heads, units_per_bh);
+  const int grid = static_cast<int>(total < n_sm ? total : n_sm);  // one persistent CTA per SM
+  auto kern = (p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true> : prefill_fwd_kernel<D, false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B,
+                                              p.Hq, p.Hkv, p.Nq, p.Nk, p.causal, p.scale_log2, pair_heads,
+                                              units_per_bh, static_cast<int>(total));
   return cudaGetLastError();
 }
 

@@ -57,6 +57,12 @@ def test_tiny_workload_full():
     (1, 1, 1, 129, 1, 128, True),
     (3, 2, 2, 128, 128, 64, True),      # exactly one tile
     (1, 4, 4, 640, 640, 128, False),
+    # more work units than SMs, so each persistent CTA runs several units;
+    # odd query-tile counts leave the second tile of some units inactive
+    (3, 40, 40, 300, 300, 128, True),
+    (3, 40, 40, 300, 300, 64, False),
+    (2, 32, 8, 700, 700, 128, True),    # GQA head pairs, 192 units
+    (2, 96, 32, 130, 390, 128, True),   # group size 3: consecutive row tiles
 ])
 def test_small_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
     q, k, v = workloads.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=100 + Nq + Nk)
@@ -72,8 +78,9 @@ def test_negative_zero_and_large_scale(scale):
         _full_check(q, k, v, causal, scale, "scale %g causal=%d" % (scale, causal))
 
 
-def test_no_keys_gives_zero_and_minus_inf():
-    q, k, v = workloads.prefill_inputs(1, 2, 2, 130, 0, 64, seed=7)
+@pytest.mark.parametrize("B,H,Nq", [(1, 2, 130), (2, 100, 300)])
+def test_no_keys_gives_zero_and_minus_inf(B, H, Nq):
+    q, k, v = workloads.prefill_inputs(B, H, H, Nq, 0, 64, seed=7)
     o, lse = _run(q, k, v, False, 0.125)
     assert torch.count_nonzero(o).item() == 0
     assert torch.isneginf(lse).all()
