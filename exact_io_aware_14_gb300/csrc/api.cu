@@ -126,6 +126,7 @@ attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const void* v_c
   if (B > 65535) return ATTN_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   if (static_cast<long long>(Hkv) * ((G + 3) / 4) > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((max_seqlen + static_cast<long long>(chunk) - 1) / chunk > 65535) return ATTN_ERR_UNSUPPORTED;  // grid z
   if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))

@@ -96,12 +96,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int split = blockIdx.x;
+  // grid (KV head x head block, batch, split), splits launched highest first:
+  // only long sequences have high splits, and every sequence's low splits
+  // are full chunks, so the last wave is made of equal full-size items
+  const int split = n_split - 1 - blockIdx.z;
   const int G = Hq / Hkv;
   const int n_hblk = (G + HPC - 1) / HPC;
-  const int hkv = blockIdx.y / n_hblk;
-  const int hb = blockIdx.y % n_hblk;
-  const int b = blockIdx.z;
+  const int hkv = blockIdx.x / n_hblk;
+  const int hb = blockIdx.x % n_hblk;
+  const int b = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   // the combine kernel may be scheduled now; it waits for this grid to finish
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   int Lb = seqlens[b];
   if (Lb < 0 || Lb > max_seqlen) {
-    if (tid == 0 && split == 0 && blockIdx.y == 0) record(1, kDevBadSeqlen);
+    if (tid == 0 && split == 0 && blockIdx.x == 0) record(1, kDevBadSeqlen);
     Lb = Lb < 0 ? 0 : max_seqlen;
   }
   const int k0 = split * chunk;
@@ -400,7 +403,7 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t stream) {
   const int n_hblk = (G + HPC - 1) / HPC;
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_split, p.Hkv * n_hblk, p.B);
+  dim3 grid(p.Hkv * n_hblk, p.B, p.n_split);
   decode_split_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(
       p.tm_k, p.tm_v, static_cast<const __nv_bfloat16*>(p.q), p.seqlens, p.max_seqlen, p.Hq, p.Hkv, p.chunk,
       p.n_split, p.scale_log2, p.o_part, p.lse_part);
