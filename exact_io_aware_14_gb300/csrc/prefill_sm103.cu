@@ -334,7 +334,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (ok && n_kt > 0) ok = wait_one(bar_full + item_base % NS, (item_base / NS) & 1, abort_flag, 4);  // K_0
-        for (int j = 0; ok && j <= n_kt; ++j) {
+        // Steps 2 .. n_both-2, where both tiles do P.V and QK^T and no per-unit
+        // barrier is due, run in a branch-free loop (below); the others in the
+        // general form.  Every instruction of this thread between two MMA
+        // batches leaves the tensor core idle, so the loop keeps ring positions
+        // and barrier parities incrementally and probes the next step's K / V
+        // before its P wait.
+        const int n_both = min(u.ti[0].n_kt, u.ti[1].n_kt);
+        const int j_steady_end = n_both - 2;
+        for (int j = 0; ok && j <= n_kt;) {
+          if (j >= 2 && j <= j_steady_end) {
+            // ring items: K_j = g, V_{j-1} = g+1, K_{j+1} = g+2, V_j = g+3
+            const uint32_t g = item_base + 2 * j - 1;
+            int s0 = static_cast<int>(g % NS);
+            uint32_t ph0 = (g / NS) & 1u;
+            uint32_t pp0 = static_cast<uint32_t>(kc[0] + j - 1) & 1u;
+            uint32_t pp1 = static_cast<uint32_t>(kc[1] + j - 1) & 1u;
+            for (; j <= j_steady_end; ++j) {
+              int s1 = s0 + 1;
+              uint32_t ph1 = ph0;
+              if (s1 >= NS) { s1 -= NS; ph1 ^= 1u; }
+              int s2 = s1 + 1;
+              uint32_t ph2 = ph1;
+              if (s2 >= NS) { s2 -= NS; ph2 ^= 1u; }
+              int s3 = s2 + 1;
+              uint32_t ph3 = ph2;
+              if (s3 >= NS) { s3 -= NS; ph3 ^= 1u; }
+              const bool k_ready = mbar_test_wait(bar_full + s2, ph2);
+              const bool v_ready = mbar_test_wait(bar_full + s3, ph3);
+              const uint64_t dv = dV + static_cast<uint64_t>((s1 * L::kTile) >> 4);
+              const uint64_t db = dK + static_cast<uint64_t>((s0 * L::kTile) >> 4);
+              if (!wait_one(bar_pfull + 0, pp0, abort_flag, 6)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_bf16_ts(tmem + 256, tmem + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, 1u);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
+                mma_bf16_ss(tmem, dQ + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(bar_sfull + 0);
+              if (!k_ready && !wait_one(bar_full + s2, ph2, abort_flag, 4)) { ok = false; break; }
+              if (!v_ready && !wait_one(bar_full + s3, ph3, abort_flag, 5)) { ok = false; break; }
+              if (!wait_one(bar_pfull + 1, pp1, abort_flag, 6)) { ok = false; break; }
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_bf16_ts(tmem + 384, tmem + 128 + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, 1u);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
+                mma_bf16_ss(tmem + 128, dQ + ((L::kTile) >> 4) + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(bar_sfull + 1);
+              s0 = s2;
+              ph0 = ph2;
+              pp0 ^= 1u;
+              pp1 ^= 1u;
+            }
+            continue;
+          }
           const uint32_t ki = item_base + k_item(j), vi = item_base + (j >= 1 ? v_item(j - 1, n_kt) : 0);
           const int ks = ki % NS, vs = vi % NS;
 #pragma unroll
@@ -379,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          ++j;
         }
         kc[0] += u.ti[0].n_kt;
         kc[1] += u.ti[1].n_kt;
