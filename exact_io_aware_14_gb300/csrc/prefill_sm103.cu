@@ -4,13 +4,15 @@
 // consecutive row tiles of one head, or -- when the GQA group size is even --
 // the same row tile of two query heads that read the same KV head (equal
 // causal extents).  Twelve warps:
-//   warp 0        TMA producer: Q0, Q1 once, then K/V tiles into one ring of
-//                 shared-memory slots in the order the MMA thread uses them
+//   warp 0        TMA producer: per work unit Q_0, Q_1, then its K/V tiles
+//                 into one ring of shared-memory slots in the order the MMA
+//                 thread uses them
 //   warp 1        TMEM allocator and MMA issuer (one thread), per key tile j:
 //                   O_0 += P_0 V_{j-1};  S_0 = Q_0 K_j^T;
 //                   O_1 += P_1 V_{j-1};  S_1 = Q_1 K_j^T
 //                 so the tensor core works on one tile while the softmax
-//                 warpgroup of the other tile runs (ping-pong).
+//                 warpgroup of the other tile runs (ping-pong); a commit
+//                 after the last MMA that reads a ring slot frees it.
 //   warps 4-7     softmax of tile 0, warps 8-11 softmax of tile 1: one
 //                 thread owns one query row (one TMEM lane); it reads its
 //                 128 scores, updates the running max m and sum l, rescales
@@ -82,8 +84,8 @@ __device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, volatil
 }
 
 // Ring order of the K/V tiles of a unit with n key tiles: K_0, then K_m,
-// V_{m-1} for m = 1 .. n-1, then V_{n-1}; MMA step j uses K_j and V_{j-1} and
-// releases both, so slots are released in ring order.
+// V_{m-1} for m = 1 .. n-1, then V_{n-1}; MMA step j uses K_j and V_{j-1}.
+// K_j is loaded two steps ahead of its use, V_{j-1} one step ahead.
 __device__ __forceinline__ int k_item(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int v_item(int j, int n) { return j == n - 1 ? 2 * n - 1 : 2 * j + 2; }
 
@@ -344,7 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j_steady_end = n_both - 2;
         for (int j = 0; ok && j <= n_kt;) {
           if (j >= 2 && j <= j_steady_end) {
-            // ring items: K_j = g, V_{j-1} = g+1, K_{j+1} = g+2, V_j = g+3
+            // ring items: K_j = g, V_{j-1} = g+1, K_{j+1} = g+2.  V_{j-1} was
+            // loaded only after S_1(j-2) was complete, so it is awaited here,
+            // right before its first use, a step after the general form
+            // would; K_{j+1} is probed now and awaited after tile 0's MMAs.
             const uint32_t g = item_base + 2 * j - 1;
             int s0 = static_cast<int>(g % NS);
             uint32_t ph0 = (g / NS) & 1u;
@@ -357,13 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               int s2 = s1 + 1;
               uint32_t ph2 = ph1;
               if (s2 >= NS) { s2 -= NS; ph2 ^= 1u; }
-              int s3 = s2 + 1;
-              uint32_t ph3 = ph2;
-              if (s3 >= NS) { s3 -= NS; ph3 ^= 1u; }
               const bool k_ready = mbar_test_wait(bar_full + s2, ph2);
-              const bool v_ready = mbar_test_wait(bar_full + s3, ph3);
               const uint64_t dv = dV + static_cast<uint64_t>((s1 * L::kTile) >> 4);
               const uint64_t db = dK + static_cast<uint64_t>((s0 * L::kTile) >> 4);
+              if (!wait_one(bar_full + s1, ph1, abort_flag, 5)) { ok = false; break; }
               if (!wait_one(bar_pfull + 0, pp0, abort_flag, 6)) { ok = false; break; }
               tc_fence_after();
 #pragma unroll
@@ -376,7 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               mma_commit(bar_sfull + 0);
               if (!k_ready && !wait_one(bar_full + s2, ph2, abort_flag, 4)) { ok = false; break; }
-              if (!v_ready && !wait_one(bar_full + s3, ph3, abort_flag, 5)) { ok = false; break; }
               if (!wait_one(bar_pfull + 1, pp1, abort_flag, 6)) { ok = false; break; }
               tc_fence_after();
 #pragma unroll
@@ -388,10 +389,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16_ss(tmem + 128, dQ + ((L::kTile) >> 4) + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
               }
               mma_commit(bar_sfull + 1);
+              mma_commit(bar_empty + s1);  // V_{j-1}: both P.V done
+              mma_commit(bar_empty + s0);  // K_j: both QK^T done
               s0 = s2;
               ph0 = ph2;
               pp0 ^= 1u;
               pp1 ^= 1u;
+            }
+            if (ok) {
+              // the general form expects V_{j-1} (the item after K_j) to have
+              // been awaited in step j-1
+              int s1 = s0 + 1;
+              uint32_t ph1 = ph0;
+              if (s1 >= NS) { s1 -= NS; ph1 ^= 1u; }
+              ok = wait_one(bar_full + s1, ph1, abort_flag, 5);
             }
             continue;
           }
@@ -413,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 0; kk < BN / 16; ++kk)
                 mma_bf16_ts(tO, tS + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
               if (j == n_t) mma_commit(bar_odone + t);
+              // the last P.V of the step: V_{j-1}'s slot is free once it completes
+              if (t == 1 || j - 1 >= u.ti[1].n_kt) mma_commit(bar_empty + vs);
             }
             if (j < n_t) {
               // S_t = Q_t K_j^T (after the P.V that read P_t: MMAs run in issue order)
@@ -425,6 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               mma_commit(bar_sfull + t);
               if (j == n_t - 1) mma_commit(bar_qfree + t);
+              // the last QK^T of the step: K_j's slot is free once it completes
+              if (t == 1 || j >= u.ti[1].n_kt) mma_commit(bar_empty + ks);
             }
             if (t == 0) {
               // the operands of step j+1 (K_{j+1}, V_j), awaited while the tensor
@@ -459,7 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // max logic is the same
     const float c = kNeg ? -scale_log2 : scale_log2;
     const bool o_32b_aligned = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-    uint32_t item_base = 0;
     int kc = 0, uc = 0;
     bool ok = true;
     for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
@@ -469,20 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo me = t ? u.ti[1] : u.ti[0];
       const int grow = me.row0 + r;
       const int my_kt = me.n_kt;
-      // The tile with more key tiles (tile 1 on a tie) releases the ring slots:
-      // once its S_j is complete, every MMA issued before its QK^T of step j --
-      // all reads of K_j and of V_{j-1} -- has completed; V_{n-1} is released
-      // after its last P.V.
-      const bool releaser = (my_kt == u.n_kt) && (t == 1 || u.ti[1].n_kt < u.n_kt) && r == 0 && my_kt > 0;
       float m = -INFINITY;  // exponent reference of this row (sign-adjusted raw score units)
       float l = 0.f;        // running sum of 2^(s*c - m*c)
       for (int j = 0; j < my_kt; ++j) {
         if (!wait_all(bar_sfull + t, (kc + j) & 1, abort_flag, 7)) { ok = false; break; }
         tc_fence_after();
-        if (releaser) {
-          mbar_arrive(bar_empty + (item_base + k_item(j)) % NS);
-          if (j >= 1) mbar_arrive(bar_empty + (item_base + v_item(j - 1, u.n_kt)) % NS);
-        }
         const int kbase = j * BN;
         const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0);
         int lim = BN;  // columns [lim, BN) of this tile are masked for this row
@@ -531,7 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------------- epilogue
       if (!wait_all(bar_odone + t, uc & 1, abort_flag, 8)) { ok = false; break; }
       tc_fence_after();
-      if (releaser) mbar_arrive(bar_empty + (item_base + 2 * u.n_kt - 1) % NS);  // V_{n-1}
       const bool store = me.row0 < Nq && grow < Nq;
       __nv_bfloat16* orow = out + ((static_cast<size_t>(u.b) * Nq + grow) * Hq + me.hq) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -571,7 +575,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         lse_out[(static_cast<size_t>(u.b) * Hq + me.hq) * Nq + grow] = lse;
       }
       kc += my_kt;
-      item_base += 2 * u.n_kt;
       ++uc;
     }
   }
