@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         qf[h][8 * cc + 6] = bf16lo(raw.w); qf[h][8 * cc + 7] = bf16hi(raw.w);
       }
     }
-    float m = -INFINITY, l = 0.f;  // running state of head `warp`
+    float m = -INFINITY, l = 0.f;  // reference of head `warp`; this lane's part of its sum
     int t_stop = n_t;
     for (int t = 0; t < n_t; ++t) {
       const int s = t % kStages;
@@ -245,24 +245,33 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (t >= 2 && !wait_all(bar_pfree + buf, ((t - 2) >> 1) & 1, abort_flag)) {
         if (lane == 0) record(3, kDevTimeout);
       }
-      // online softmax of head `warp` over this tile's 64 scores
+      // online softmax of head `warp` over this tile's 64 scores.  The
+      // reference only has to move when a score exceeds it by more than
+      // 2^kRescaleLog2, which each lane checks for its own two scores (one
+      // vote); only then is the tile max formed.  Each lane keeps its own part
+      // of the sum l; the parts are added once, at the end of the split.
       {
         const float x0 = sS[(buf * HPC + warp) * KT + lane], x1 = sS[(buf * HPC + warp) * KT + lane + 32];
-        float mt = fmaxf(x0, x1);
+        const float mc_old = (m == -INFINITY) ? 0.f : m * c;
+        const bool big = (m == -INFINITY) || (fmaf(x0, c, -mc_old) > kRescaleLog2) ||
+                         (fmaf(x1, c, -mc_old) > kRescaleLog2);
+        float alpha = 1.f;
+        float mc = mc_old;
+        if (__any_sync(0xffffffffu, big)) {
+          float mt = fmaxf(x0, x1);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-        const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
-        const float m_new = need ? fmaxf(m, mt) : m;
-        const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
+          for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+          const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
+          const float m_new = need ? fmaxf(m, mt) : m;
+          mc = (m_new == -INFINITY) ? 0.f : m_new * c;
+          alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
+          l *= alpha;
+          m = m_new;
+        }
         float p0 = ex2_approx(fmaf(x0, c, -mc)), p1 = ex2_approx(fmaf(x1, c, -mc));
         p0 = (lane < valid) ? p0 : 0.f;  // also right for c == 0
         p1 = (lane + 32 < valid) ? p1 : 0.f;
-        float ps = p0 + p1;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
-        l = l * alpha + ps;
-        m = m_new;
+        l += p0 + p1;
         sP[(buf * KT + lane) * HPC + warp] = p0;
         sP[(buf * KT + lane + 32) * HPC + warp] = p1;
         if (lane == 0) sAlpha[buf * HPC + warp] = alpha;
@@ -293,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int t = t_stop; t < n_issued; ++t)
         if (!mbar_wait(bar_full + (t % kStages), (t / kStages) & 1, &no_abort, kWaitLimitNs)) break;
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     if (lane == 0) {
       sM[warp] = m;
       sL[warp] = l;

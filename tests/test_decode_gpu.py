@@ -50,6 +50,22 @@ def test_chunk_sizes(chunk):
     _check(q, k, v, L, 0.0884, chunk, "chunk%d" % chunk)
 
 
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_rising_scores_move_the_reference(sign):
+    """Scores that climb by ~60 (natural-log units) along each sequence move
+    the exponent reference many times inside one split; a negative scale
+    runs the same path on -s."""
+    lens = [3000, 1500, 700]
+    B, Hq, Hkv, d, N = len(lens), 8, 2, 128, 3072
+    q, k, v, L = workloads.decode_inputs(B, Hq, Hkv, N, d, 0, 0, seed=42, seqlens=lens)
+    q = torch.ones_like(q)
+    ramp = torch.zeros((B, N), dtype=torch.float32)
+    for b, n in enumerate(lens):
+        ramp[b, :n] = torch.linspace(-4.0, 4.0, n)
+    k = (ramp[:, :, None, None] * torch.ones((1, 1, Hkv, d))).to(torch.bfloat16)
+    _check(q, k, v, L, sign * d ** -0.5, 1024, "rising scores sign %+d" % sign)
+
+
 def test_zero_length_sequence():
     lens = [0, 17]
     q, k, v, L = workloads.decode_inputs(2, 4, 2, 128, 128, 0, 0, seed=41, seqlens=lens)
