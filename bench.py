@@ -214,6 +214,28 @@ def oracle_sample_rate(w, q, k, v, seqlens, budget_s, seed):
 
 
 # --------------------------------------------------------------------------- our arm
+def max_over_ranks(x, world):
+    """Largest value of x over all ranks: the whole job is as slow as its
+    slowest rank.  Works under NCCL (device tensor) and gloo (host tensor)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    if dist.get_backend() == "gloo":
+        dev = torch.device("cpu")
+    else:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def whole_job_rate(work_per_rank, ms_per_step, world, scale_unit):
+    """Units every rank processed in one step over the (slowest) step time:
+    N independent replicas each do `work_per_rank` per step (weak scaling)."""
+    return world * work_per_rank / (ms_per_step * 1e-3) / scale_unit
+
+
 def run_ours(args, w, rank, world, local_rank):
     import torch
     from exact_io_aware_14_gb300 import _native, build as native_build, workloads as W
@@ -301,13 +323,9 @@ def run_ours(args, w, rank, world, local_rank):
     if _native.attn_get_device_status(stream) != 0:
         raise RuntimeError("device status error in the timed region")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = t.item()
+    total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
-    value = world * work / (ms_per_step * 1e-3) / scale_unit
+    value = whole_job_rate(work, ms_per_step, world, scale_unit)
     kernel_rate = work / (statistics.mean(step_ms) * 1e-3) / scale_unit
 
     # ---- e2e through host buffers (pinned), copies inside the timed region
@@ -339,12 +357,8 @@ def run_ours(args, w, rank, world, local_rank):
         e2e_step()
         ee[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = t.item()
-    e2e_value = world * work / (e2e_ms * 1e-3) / scale_unit
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps, world)
+    e2e_value = whole_job_rate(work, e2e_ms, world, scale_unit)
 
     if rank != 0:
         return None
