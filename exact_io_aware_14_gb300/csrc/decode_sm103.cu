@@ -85,6 +85,61 @@ __device__ __forceinline__ bool score_bar_or(bool v) {
   return r != 0;
 }
 
+// Work order for up to kRankB sequences: the CTAs (in launch order) take
+// every sequence's full splits first and the shorter last splits after them,
+// longest first, so the last CTAs to start are the shortest.  Warp 0 lists
+// the splits from seqlens (lanes hold sequences lane and lane+32) and picks
+// item i; returns (b, split), or b = -1 when i is past the last split.
+constexpr int kRankB = 64;
+__device__ __forceinline__ int2 pick_item(const int* __restrict__ seqlens, int B, int max_seqlen, int chunk, int i,
+                                          int lane) {
+  int L[2], nf[2], rem[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int b = lane + 32 * k;
+    int v = b < B ? seqlens[b] : 0;
+    v = v < 0 ? 0 : (v > max_seqlen ? max_seqlen : v);
+    L[k] = v;
+    nf[k] = v / chunk;
+    rem[k] = v % chunk;
+  }
+  // full splits, sequence after sequence: exclusive prefix of nf over b
+  int incl0 = nf[0], incl1 = nf[1];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y0 = __shfl_up_sync(0xffffffffu, incl0, o), y1 = __shfl_up_sync(0xffffffffu, incl1, o);
+    if (lane >= o) {
+      incl0 += y0;
+      incl1 += y1;
+    }
+  }
+  const int tot0 = __shfl_sync(0xffffffffu, incl0, 31);
+  incl1 += tot0;
+  const int n_full = __shfl_sync(0xffffffffu, incl1, 31);
+  int2 r = make_int2(-1, 0);
+  if (i < n_full) {
+    if (incl0 - nf[0] <= i && i < incl0) r = make_int2(lane, i - (incl0 - nf[0]));
+    if (incl1 - nf[1] <= i && i < incl1) r = make_int2(lane + 32, i - (incl1 - nf[1]));
+  } else {
+    // last splits shorter than the chunk, ranked by length (longest first), then b
+    const int j = i - n_full;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      int rank = 0;
+      for (int b2 = 0; b2 < B; ++b2) {
+        const int r2 = __shfl_sync(0xffffffffu, rem[b2 >> 5], b2 & 31);
+        rank += (r2 > rem[k] || (r2 == rem[k] && b2 < lane + 32 * k)) ? 1 : 0;
+      }
+      if (rem[k] > 0 && rank == j) r = make_int2(lane + 32 * k, nf[k]);
+    }
+  }
+  // the (single) lane that found the item broadcasts it
+  const unsigned found = __ballot_sync(0xffffffffu, r.x >= 0);
+  if (found == 0u) return make_int2(-1, 0);
+  const int src = __ffs(found) - 1;
+  return make_int2(__shfl_sync(0xffffffffu, r.x, src), __shfl_sync(0xffffffffu, r.y, src));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -96,23 +151,35 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  // grid (KV head x head block, batch, split), splits launched highest first:
-  // only long sequences have high splits, and every sequence's low splits
-  // are full chunks, so the last wave is made of equal full-size items
-  const int split = n_split - 1 - blockIdx.z;
+  // grid (KV head x head block, batch, split).  Up to kRankB sequences the
+  // CTA with linear item index (z, y) takes the item pick_item lists there;
+  // beyond that, splits are launched highest first (only long sequences
+  // have high splits, and every sequence's low splits are full chunks).
   const int G = Hq / Hkv;
   const int n_hblk = (G + HPC - 1) / HPC;
   const int hkv = blockIdx.x / n_hblk;
   const int hb = blockIdx.x % n_hblk;
-  const int b = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   // the combine kernel may be scheduled now; it waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  const int B = gridDim.y;
+  int b = blockIdx.y, split = n_split - 1 - blockIdx.z;
+  if (B <= kRankB) {
+    __shared__ int2 s_item;
+    if (warp == 0) {
+      const int2 it = pick_item(seqlens, B, max_seqlen, chunk, blockIdx.z * B + blockIdx.y, lane);
+      if (lane == 0) s_item = it;
+    }
+    __syncthreads();
+    b = s_item.x;
+    split = s_item.y;
+    if (b < 0) return;  // past the last split
+  }
   int Lb = seqlens[b];
   if (Lb < 0 || Lb > max_seqlen) {
-    if (tid == 0 && split == 0 && blockIdx.x == 0) record(1, kDevBadSeqlen);
+    if (tid == 0 && blockIdx.x == 0) record(1, kDevBadSeqlen);
     Lb = Lb < 0 ? 0 : max_seqlen;
   }
   const int k0 = split * chunk;

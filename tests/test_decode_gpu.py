@@ -66,6 +66,17 @@ def test_rising_scores_move_the_reference(sign):
     _check(q, k, v, L, sign * d ** -0.5, 1024, "rising scores sign %+d" % sign)
 
 
+@pytest.mark.parametrize("B", [33, 64, 70])
+def test_many_sequences(B):
+    """Work order across the batch: lanes of both halves of the listing warp
+    (B > 32), the largest batch it lists (64), and the plain order beyond."""
+    g = torch.Generator().manual_seed(43 + B)
+    lens = torch.randint(0, 300, (B,), generator=g).tolist()
+    lens[0], lens[-1] = 256, 0
+    q, k, v, L = workloads.decode_inputs(B, 4, 2, 320, 64, 0, 0, seed=44 + B, seqlens=lens)
+    _check(q, k, v, L, 0.125, 64, "B%d" % B)
+
+
 def test_zero_length_sequence():
     lens = [0, 17]
     q, k, v, L = workloads.decode_inputs(2, 4, 2, 128, 128, 0, 0, seed=41, seqlens=lens)
