@@ -14,9 +14,11 @@
 //              and a 3-level shuffle reduction; then one warp per head runs
 //              the online softmax (exponent reference moved only when the max
 //              rises by more than 2^8, as in the prefill kernel) and writes
-//              P.  Thread 0 also issues the TMA loads.
+//              P.
 //   warps 4-7  P.V: each thread owns 4 output dims of the 4 heads for a
-//              quarter of the keys, packed fp32x2 FMAs.
+//              quarter of the keys, packed fp32x2 FMAs.  Lane 0 of warp 4
+//              issues the TMA loads, refilling a stage as soon as its P.V is
+//              done.
 // The CTA writes its split's normalised partial output and natural-log LSE.
 // Decode is memory-bound ("FlashAttention: Part 2", section 4.1): the kernel
 // exists to keep ~128 KB of loads in flight per SM with few instructions per
@@ -93,13 +95,12 @@ __device__ __forceinline__ bool score_bar_or(bool v) {
 constexpr int kRankB = 64;
 __device__ __forceinline__ int2 pick_item(const int* __restrict__ seqlens, int B, int max_seqlen, int chunk, int i,
                                           int lane) {
-  int L[2], nf[2], rem[2];
+  int nf[2], rem[2];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int b = lane + 32 * k;
     int v = b < B ? seqlens[b] : 0;
     v = v < 0 ? 0 : (v > max_seqlen ? max_seqlen : v);
-    L[k] = v;
     nf[k] = v / chunk;
     rem[k] = v % chunk;
   }
@@ -216,25 +217,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool negate = scale_log2 < 0.f;
   const float c = negate ? -scale_log2 : scale_log2;
 
+  // Loads are issued by lane 0 of warp 4 (the first P.V warp): the first
+  // kStages tiles now, then each stage again as soon as its P.V is done.
+  auto issue = [&](int t) {
+    const int s = t % kStages;
+    const int key = k0 + t * KT;
+    mbar_arrive_expect_tx(bar_full + s, 2 * L::kTile);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_full + s, h * 64, hkv, key, b);
+      tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_full + s, h * 64, hkv, key, b);
+    }
+  };
+  const bool loader = (tid == kScoreThreads);
+  int n_issued = 0;  // meaningful in the loader only
+  if (loader) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    for (int t = 0; t < n_t && t < kStages; ++t) issue(t);
+    n_issued = min(n_t, kStages);
+  }
+
   if (warp < 4) {
     // ================================================================ scores + softmax
-    auto issue = [&](int t) {
-      const int s = t % kStages;
-      const int key = k0 + t * KT;
-      mbar_arrive_expect_tx(bar_full + s, 2 * L::kTile);
-#pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_full + s, h * 64, hkv, key, b);
-        tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_full + s, h * 64, hkv, key, b);
-      }
-    };
-    int n_issued = 0;  // meaningful in thread 0 only
-    if (tid == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      for (int t = 0; t < n_t && t < kStages; ++t) issue(t);
-      n_issued = min(n_t, kStages);
-    }
     // key slot ks (keys ks, ks+16, ks+32, ks+48), 16-byte chunk dseg of each
     // 64-column half of the key row
     const int ks = tid >> 3;
@@ -254,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     float m = -INFINITY, l = 0.f;  // reference of head `warp`; this lane's part of its sum
-    int t_stop = n_t;
     for (int t = 0; t < n_t; ++t) {
       const int s = t % kStages;
       const int buf = t & 1;
@@ -303,7 +307,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (score_bar_or(!got || *abort_flag)) {
         if (tid == 0) record(2, kDevTimeout);
         *abort_flag = 1;
-        t_stop = t;
         break;
       }
       // P buffer `buf` is free once the P.V of tile t-2 is done.  A failed
@@ -353,21 +356,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pfull + buf);
-      // refill the stage of tile t-1 once its P.V is done
-      if (warp == 0 && t >= 1 && t - 1 + kStages < n_t) {
-        if (!wait_all(bar_pfree + ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag)) {
-          if (lane == 0) record(4, kDevTimeout);
-        } else if (lane == 0) {
-          issue(t - 1 + kStages);
-          n_issued = t + kStages;
-        }
-      }
-    }
-    if (warp == 0 && lane == 0 && *abort_flag) {
-      // every issued load must land before the CTA may exit (bounded, not abortable)
-      volatile int no_abort = 0;
-      for (int t = t_stop; t < n_issued; ++t)
-        if (!mbar_wait(bar_full + (t % kStages), (t / kStages) & 1, &no_abort, kWaitLimitNs)) break;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -417,6 +405,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pfree + buf);
+      // refill this tile's stage once all four P.V warps are done with it (the
+      // score warps finished with its K before marking P ready)
+      if (warp == 4 && t + kStages < n_t) {
+        if (!wait_all(bar_pfree + buf, (t >> 1) & 1, abort_flag)) {
+          if (lane == 0) record(4, kDevTimeout);
+          break;
+        }
+        if (lane == 0) {
+          issue(t + kStages);
+          n_issued = t + kStages + 1;
+        }
+      }
+    }
+    if (loader && *abort_flag) {
+      // every issued load must land before the CTA may exit (bounded, not abortable)
+      volatile int no_abort = 0;
+      for (int t = n_issued > kStages ? n_issued - kStages : 0; t < n_issued; ++t)
+        if (!mbar_wait(bar_full + (t % kStages), (t / kStages) & 1, &no_abort, kWaitLimitNs)) break;
     }
 #pragma unroll
     for (int h = 0; h < HPC; ++h) {
