@@ -149,7 +149,7 @@ class ClockSampler:
 def get_workload(name):
     from exact_io_aware_14_gb300 import workloads as W
     table = {"tiny": W.TINY, "train_causal": W.TRAIN_CAUSAL, "train": W.TRAIN, "gqa": W.GQA, "long": W.LONG,
-             "decode": W.DECODE}
+             "decode": W.DECODE, "decode_paged": W.DECODE_PAGED}
     return table[name]
 
 
@@ -158,6 +158,9 @@ def config_of(w, n_gpus):
     if isinstance(w, W.Decode):
         cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "max_seqlen": w.max_seqlen, "d": w.d,
                "chunk": w.chunk, "seqlens": "U[%d,%d] int32, seed %d" % (w.len_lo, w.len_hi, w.seed)}
+        if w.page_size:
+            cfg["page_size"] = w.page_size
+            cfg["pages"] = "shuffled page pool, block table [B, max_seqlen/page_size]"
     else:
         cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.N, "Nk": w.N, "d": w.d,
                "causal": w.causal, "scale": "1/sqrt(d)"}
@@ -276,11 +279,31 @@ def run_ours(args, w, rank, world, local_rank):
         work = decode_bytes(w, L_host)
         unit, scale_unit = "GB/s", 1e9
         launches_per_step = 2
+        if w.page_size:
+            # the same logical cache in a shuffled page pool (one spare page)
+            mb = w.max_seqlen // w.page_size
+            n_pages = w.B * mb + 1
+            block_table = torch.randperm(n_pages, generator=gen, device=dev)[: w.B * mb].to(torch.int32)
+            block_table = block_table.reshape(w.B, mb).contiguous()
+            k_pages = torch.empty((n_pages, w.page_size, w.Hkv, w.d), dtype=torch.bfloat16, device=dev)
+            v_pages = torch.empty_like(k_pages)
+            idx = block_table.reshape(-1).long()
+            k_pages[idx] = k.reshape(w.B * mb, w.page_size, w.Hkv, w.d)
+            v_pages[idx] = v.reshape(w.B * mb, w.page_size, w.Hkv, w.d)
+            dev_inputs = [q, k_pages, v_pages, block_table, seqlens]
 
-        def step():
-            rc = _native.attn_fwd_splitkv(q, k, v, seqlens, o, lse, w.scale, w.chunk, ws, stream)
-            if rc != 0:
-                raise RuntimeError("attn_fwd_splitkv: %s" % _native.status_string(rc))
+            def step():
+                rc = _native.attn_fwd_splitkv_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, w.scale,
+                                                    w.chunk, ws, stream)
+                if rc != 0:
+                    raise RuntimeError("attn_fwd_splitkv_paged: %s" % _native.status_string(rc))
+        else:
+            dev_inputs = [q, k, v, seqlens]
+
+            def step():
+                rc = _native.attn_fwd_splitkv(q, k, v, seqlens, o, lse, w.scale, w.chunk, ws, stream)
+                if rc != 0:
+                    raise RuntimeError("attn_fwd_splitkv: %s" % _native.status_string(rc))
     else:
         q = randn((w.B, w.N, w.Hq, w.d), w.amp)
         k = randn((w.B, w.N, w.Hkv, w.d), w.amp)
@@ -330,8 +353,8 @@ def run_ours(args, w, rank, world, local_rank):
 
     # ---- e2e through host buffers (pinned), copies inside the timed region
     if dec:
-        h_in = [x.cpu().pin_memory() for x in (q, k, v, seqlens)]
-        d_in = [q, k, v, seqlens]
+        h_in = [x.cpu().pin_memory() for x in dev_inputs]
+        d_in = dev_inputs
         h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (o, lse)]
     else:
         h_in = [x.cpu().pin_memory() for x in (q, k, v)]
@@ -438,7 +461,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="train_causal",
-                    choices=["tiny", "train_causal", "train", "gqa", "long", "decode"])
+                    choices=["tiny", "train_causal", "train", "gqa", "long", "decode", "decode_paged"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--reference-seconds", type=float, default=90.0, help="whole reference-arm budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")

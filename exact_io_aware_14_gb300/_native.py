@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libattn_sm103.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "attn.h")
 
 ATTN_OK = 0
+ATTN_ERR_DEVICE_ARG = 6
 STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
     4: "ATTN_ERR_LAUNCH", 5: "ATTN_ERR_TIMEOUT", 6: "ATTN_ERR_DEVICE_ARG", 7: "ATTN_ERR_WORKSPACE",
@@ -49,6 +50,8 @@ def lib():
         L.attn_splitkv_workspace_size.argtypes = [i, i, i, i, i]
         L.attn_fwd_splitkv.restype = i
         L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+        L.attn_fwd_splitkv_paged.restype = i
+        L.attn_fwd_splitkv_paged.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
         L.attn_fwd_splitkv_noalloc.restype = i
         L.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp]
         L.attn_get_device_status.restype = i
@@ -116,6 +119,29 @@ def attn_fwd_splitkv(q, k_cache, v_cache, seqlens, o, lse, scale, chunk, workspa
                                   _stream_handle(stream))
 
 
+def attn_fwd_splitkv_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, scale, chunk, workspace, stream=None):
+    """Same contract as the C call: k_pages, v_pages [num_pages, page_size, Hkv, d];
+    block_table int32 [B, max_blocks] on the device.  Returns the status."""
+    B, _, Hq, d = q.shape
+    num_pages, page_size, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    max_blocks = block_table.shape[1]
+    _check_bf16("q", q, (B, 1, Hq, d))
+    _check_bf16("k_pages", k_pages, (num_pages, page_size, Hkv, d))
+    _check_bf16("v_pages", v_pages, (num_pages, page_size, Hkv, d))
+    _check_bf16("o", o, (B, 1, Hq, d))
+    if block_table.dtype != torch.int32 or not block_table.is_cuda or not block_table.is_contiguous() \
+            or tuple(block_table.shape) != (B, max_blocks):
+        raise ValueError("block_table must be a contiguous CUDA int32 tensor of shape (%d, max_blocks)" % B)
+    if seqlens.dtype != torch.int32 or not seqlens.is_cuda or tuple(seqlens.shape) != (B,):
+        raise ValueError("seqlens must be a CUDA int32 tensor of shape (%d,)" % B)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, Hq, 1):
+        raise ValueError("lse must be a CUDA fp32 tensor of shape %s" % ((B, Hq, 1),))
+    return lib().attn_fwd_splitkv_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), max_blocks,
+                                        page_size, num_pages, _ptr(seqlens), _ptr(o), _ptr(lse), B, Hq, Hkv, d,
+                                        float(scale), int(chunk), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+
+
 def attn_fwd_splitkv_noalloc(q, k_cache, v_cache, seqlens, o, lse, scale, chunk, stream=None):
     """attn_fwd_splitkv without a workspace: the library's fixed device scratch
     holds the partials, so nothing is allocated (for callers that cannot
@@ -148,6 +174,20 @@ def forward(q, k, v, causal, scale, stream=None):
     rc = attn_fwd(q, k, v, o, lse, causal, scale, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, scale, chunk=1024, workspace=None, stream=None):
+    """Allocates O, LSE (and the workspace unless given) and runs attn_fwd_splitkv_paged."""
+    B, _, Hq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = attn_splitkv_workspace_size(B, Hq, block_table.shape[1] * k_pages.shape[1], d, chunk)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    rc = attn_fwd_splitkv_paged(q, k_pages, v_pages, block_table, seqlens, o, lse, scale, chunk, workspace, stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_splitkv_paged")
     return o, lse
 
 

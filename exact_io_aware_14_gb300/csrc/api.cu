@@ -64,7 +64,7 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case ATTN_ERR_LAUNCH: return "CUDA launch or runtime error";
     case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
-    case ATTN_ERR_DEVICE_ARG: return "cache length outside [0, max_seqlen]";
+    case ATTN_ERR_DEVICE_ARG: return "cache length or page index out of range";
     case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
   }
   return "unknown status";
@@ -116,9 +116,17 @@ size_t attn_splitkv_workspace_size(int B, int Hq, int max_seqlen, int d, int chu
   return round16(parts * d * sizeof(float)) + round16(parts * sizeof(float));
 }
 
-attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
-                             int max_seqlen, void* o, float* lse, int B, int Hq, int Hkv, int d, float scale,
-                             int chunk, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the contiguous and the paged split-KV calls.  Paged: block_table
+// non-null, k/v are page pools [num_pages, page_size, Hkv, d] and the
+// logical cache capacity is max_blocks * page_size.
+attn_status splitkv(const void* q, const void* k, const void* v, const int* seqlens, int max_seqlen,
+                    const int* block_table, int max_blocks, int page_size, int num_pages, void* o, float* lse,
+                    int B, int Hq, int Hkv, int d, float scale, int chunk, void* workspace, size_t workspace_bytes,
+                    void* stream) {
   if (B < 1 || Hq < 1 || Hkv < 1 || (Hq % Hkv) != 0 || max_seqlen < 1) return ATTN_ERR_INVALID_ARG;
   if (chunk < 64 || (chunk % 64) != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -127,17 +135,25 @@ attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const void* v_c
   const int G = Hq / Hkv;
   if (static_cast<long long>(Hkv) * ((G + 3) / 4) > 65535) return ATTN_ERR_UNSUPPORTED;
   if ((max_seqlen + static_cast<long long>(chunk) - 1) / chunk > 65535) return ATTN_ERR_UNSUPPORTED;  // grid z
-  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+  if (!q || !k || !v || !seqlens || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u))
     return ATTN_ERR_MISALIGNED;
+  if (block_table) {
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u)) return ATTN_ERR_MISALIGNED;
+    // the pages of one split must fit the kernel's list of them
+    if (chunk / page_size + 2 > 128) return ATTN_ERR_UNSUPPORTED;
+  }
   const size_t need = attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
 
   attn::DecodeParams p;
   std::memset(&p, 0, sizeof p);
-  if (!make_map(&p.tm_k, k_cache, B, max_seqlen, Hkv, d, 64) || !make_map(&p.tm_v, v_cache, B, max_seqlen, Hkv, d, 64))
-    return ATTN_ERR_LAUNCH;
+  const bool ok_maps = block_table ? (make_map(&p.tm_k, k, num_pages, page_size, Hkv, d, 64) &&
+                                      make_map(&p.tm_v, v, num_pages, page_size, Hkv, d, 64))
+                                   : (make_map(&p.tm_k, k, B, max_seqlen, Hkv, d, 64) &&
+                                      make_map(&p.tm_v, v, B, max_seqlen, Hkv, d, 64));
+  if (!ok_maps) return ATTN_ERR_LAUNCH;
   p.n_split = (max_seqlen + chunk - 1) / chunk;
   const size_t parts = splitkv_part_elems(B, Hq, p.n_split);
   p.o_part = static_cast<float*>(workspace);
@@ -146,6 +162,10 @@ attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const void* v_c
   p.seqlens = seqlens;
   p.o = o;
   p.lse = lse;
+  p.block_table = block_table;
+  p.max_blocks = max_blocks;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -154,6 +174,29 @@ attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const void* v_c
   p.chunk = chunk;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   return attn::launch_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+                             int max_seqlen, void* o, float* lse, int B, int Hq, int Hkv, int d, float scale,
+                             int chunk, void* workspace, size_t workspace_bytes, void* stream) {
+  return splitkv(q, k_cache, v_cache, seqlens, max_seqlen, nullptr, 0, 0, 0, o, lse, B, Hq, Hkv, d, scale, chunk,
+                 workspace, workspace_bytes, stream);
+}
+
+attn_status attn_fwd_splitkv_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                                   int max_blocks, int page_size, int num_pages, const int* seqlens, void* o,
+                                   float* lse, int B, int Hq, int Hkv, int d, float scale, int chunk, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!block_table || max_blocks < 1 || num_pages < 1 || page_size < 64 || (page_size % 64) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  const long long cap = static_cast<long long>(max_blocks) * page_size;
+  if (cap > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  return splitkv(q, k_pages, v_pages, seqlens, static_cast<int>(cap), block_table, max_blocks, page_size, num_pages,
+                 o, lse, B, Hq, Hkv, d, scale, chunk, workspace, workspace_bytes, stream);
 }
 
 attn_status attn_get_device_status(void* stream) {
@@ -166,7 +209,8 @@ attn_status attn_get_device_status(void* stream) {
   switch (w & 0xffu) {
     case 0: return ATTN_OK;
     case attn::kDevTimeout: return ATTN_ERR_TIMEOUT;
-    case attn::kDevBadSeqlen: return ATTN_ERR_DEVICE_ARG;
+    case attn::kDevBadSeqlen:
+    case attn::kDevBadPage: return ATTN_ERR_DEVICE_ARG;
     default: return ATTN_ERR_LAUNCH;
   }
 }

@@ -141,12 +141,19 @@ __device__ __forceinline__ int2 pick_item(const int* __restrict__ seqlens, int B
   return make_int2(__shfl_sync(0xffffffffu, r.x, src), __shfl_sync(0xffffffffu, r.y, src));
 }
 
-template <int D>
+// Paged cache: the pages of one split, at most this many.
+constexpr int kMaxSplitPages = 128;
+
+// kPaged: K/V live in pages [num_pages, page_size, Hkv, d]; key k of sequence
+// b is row k % page_size of page block_table[b * max_blocks + k / page_size]
+// (page_size a multiple of the 64-key tile, so a tile never spans pages).
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens, int max_seqlen,
                         int Hq, int Hkv, int chunk, int n_split, float scale_log2, float* __restrict__ o_part,
-                        float* __restrict__ lse_part) {
+                        float* __restrict__ lse_part, const int* __restrict__ block_table, int max_blocks,
+                        int page_size, int num_pages) {
   using L = DLayout<D>;
   constexpr int NCH = D / 64;  // 16-byte chunks per key that one score thread reads
   extern __shared__ uint8_t smem_raw[];
@@ -203,6 +210,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* sK = smem + L::kOffK;
   uint8_t* sV = smem + L::kOffV;
 
+  // pages of this split (paged cache): read once, before the barrier below
+  __shared__ int s_pages[kPaged ? kMaxSplitPages : 1];
+  const int p0 = kPaged ? k0 / page_size : 0;
+  if (kPaged) {
+    const int n_pg = (k0 + kn - 1) / page_size - p0 + 1;  // <= kMaxSplitPages (checked on the host)
+    for (int i = tid; i < n_pg; i += kThreads) {
+      int pg = block_table[static_cast<size_t>(b) * max_blocks + p0 + i];
+      if (pg < 0 || pg >= num_pages) {
+        record(6, kDevBadPage);
+        pg = 0;  // keep every load inside the page pool; the result is flagged
+      }
+      s_pages[i] = pg;
+    }
+  }
+
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(bar_full + s, 1);
     for (int i = 0; i < 2; ++i) {
@@ -222,11 +244,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto issue = [&](int t) {
     const int s = t % kStages;
     const int key = k0 + t * KT;
+    // (row, outer index) of the tile: (key, b), or (row in page, page) when paged
+    const int row = kPaged ? key % page_size : key;
+    const int outer = kPaged ? s_pages[key / page_size - p0] : b;
     mbar_arrive_expect_tx(bar_full + s, 2 * L::kTile);
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {
-      tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_full + s, h * 64, hkv, key, b);
-      tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_full + s, h * 64, hkv, key, b);
+      tma_load_4d(sK + s * L::kTile + h * L::kHalf, &tm_k, bar_full + s, h * 64, hkv, row, outer);
+      tma_load_4d(sV + s * L::kTile + h * L::kHalf, &tm_v, bar_full + s, h * 64, hkv, row, outer);
     }
   };
   const bool loader = (tid == kScoreThreads);
@@ -485,12 +510,14 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t stream) {
   using L = DLayout<D>;
   const int G = p.Hq / p.Hkv;
   const int n_hblk = (G + HPC - 1) / HPC;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  auto kern = p.block_table ? decode_split_kernel<D, true> : decode_split_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Hkv * n_hblk, p.B, p.n_split);
-  decode_split_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(
-      p.tm_k, p.tm_v, static_cast<const __nv_bfloat16*>(p.q), p.seqlens, p.max_seqlen, p.Hq, p.Hkv, p.chunk,
-      p.n_split, p.scale_log2, p.o_part, p.lse_part);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(p.tm_k, p.tm_v, static_cast<const __nv_bfloat16*>(p.q), p.seqlens,
+                                               p.max_seqlen, p.Hq, p.Hkv, p.chunk, p.n_split, p.scale_log2,
+                                               p.o_part, p.lse_part, p.block_table, p.max_blocks, p.page_size,
+                                               p.num_pages);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the combine grid is set up while the split

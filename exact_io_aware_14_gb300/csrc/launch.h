@@ -10,7 +10,7 @@ namespace attn {
 
 // Device status codes.  Kernels never trap: a wait that runs out of time
 // records (site << 8) | code in the unit's status word and the kernel unwinds.
-enum DeviceCode : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBadSeqlen = 6 };
+enum DeviceCode : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBadSeqlen = 6, kDevBadPage = 7 };
 
 struct PrefillParams {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, N, B}, box {64, 1, 128, 1}, 128-B swizzle
@@ -29,6 +29,9 @@ struct DecodeParams {
   float* lse;
   float* o_part;    // [B, Hq, n_split, d]
   float* lse_part;  // [B, Hq, n_split]
+  // paged cache (block_table non-null): maps are {d, Hkv, page_size, num_pages}
+  const int* block_table;  // [B, max_blocks]
+  int max_blocks, page_size, num_pages;
   int B, Hq, Hkv, d, max_seqlen, chunk, n_split;
   float scale_log2;
 };

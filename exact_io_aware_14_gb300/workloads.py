@@ -51,6 +51,7 @@ class Decode:
     len_lo: int
     len_hi: int
     seed: int = 4
+    page_size: int = 0  # > 0: the cache is paged (shuffled pages of this many keys)
 
     @property
     def scale(self) -> float:
@@ -66,6 +67,8 @@ GQA = Prefill("gqa_prefill_b2_hq32_hkv8_n8192_d128_causal", 2, 32, 8, 8192, 128,
 LONG = Prefill("long_b1_h8_n32768_d128_causal", 1, 8, 8, 32768, 128, True, seed=3)
 DECODE = Decode("decode_b16_hq32_hkv8_len1024to16384_d128_chunk1024", 16, 32, 8, 16384, 128, 1024,
                 1024, 16384, seed=4)
+DECODE_PAGED = Decode("decode_paged_b16_hq32_hkv8_len1024to16384_d128_chunk1024_page256", 16, 32, 8, 16384, 128,
+                      1024, 1024, 16384, seed=4, page_size=256)
 
 PREFILL_WORKLOADS = (TINY, TRAIN_CAUSAL, TRAIN, GQA, LONG)
 
@@ -114,6 +117,31 @@ def decode_inputs(B, Hq, Hkv, max_seqlen, d, len_lo, len_hi, seed=4, poison=True
             k[b, L:] = float("nan")
             v[b, L:] = float("nan")
     return q, k, v, seqlens
+
+
+def page_cache(k, v, page_size, extra_pages=3, seed=0):
+    """Scatter a contiguous cache [B, max_seqlen, Hkv, d] into page pools
+    [num_pages, page_size, Hkv, d] under a seeded random page order.
+
+    Returns (k_pages, v_pages, block_table int32 [B, max_blocks]); key k of
+    sequence b is row k % page_size of page block_table[b, k // page_size].
+    Pages that no sequence uses (``extra_pages`` of them) hold NaN.
+    """
+    B, S, Hkv, d = k.shape
+    max_blocks = -(-S // page_size)
+    num_pages = B * max_blocks + extra_pages
+    gen = torch.Generator().manual_seed(5000 + seed)
+    order = torch.randperm(num_pages, generator=gen)[: B * max_blocks].to(torch.int32)
+    block_table = order.reshape(B, max_blocks).contiguous()
+    k_pages = torch.full((num_pages, page_size, Hkv, d), float("nan"), dtype=k.dtype)
+    v_pages = torch.full((num_pages, page_size, Hkv, d), float("nan"), dtype=v.dtype)
+    for b in range(B):
+        for blk in range(max_blocks):
+            lo, hi = blk * page_size, min(S, (blk + 1) * page_size)
+            pg = int(block_table[b, blk])
+            k_pages[pg, : hi - lo] = k[b, lo:hi]
+            v_pages[pg, : hi - lo] = v[b, lo:hi]
+    return k_pages, v_pages, block_table
 
 
 def workload_decode_inputs(w: Decode, poison=True):

@@ -59,7 +59,7 @@ typedef enum {
   ATTN_ERR_MISALIGNED = 3,   /* a pointer is not 16-byte aligned */
   ATTN_ERR_LAUNCH = 4,       /* the CUDA runtime refused a launch or a query */
   ATTN_ERR_TIMEOUT = 5,      /* device: a pipeline wait gave up (reported later) */
-  ATTN_ERR_DEVICE_ARG = 6,   /* device: a cache length was outside [0, max_seqlen] */
+  ATTN_ERR_DEVICE_ARG = 6,   /* device: a cache length or page index was out of range */
   ATTN_ERR_WORKSPACE = 7     /* workspace missing or smaller than required */
 } attn_status;
 
@@ -114,6 +114,29 @@ ATTN_API attn_status attn_fwd_splitkv(const void* q, const void* k_cache, const 
                              void* o, float* lse,
                              int B, int Hq, int Hkv, int d, float scale, int chunk,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The same decode against a paged KV cache (pyshine.com flash-attention
+ * tour, "Why You Need This": a paged KV cache for serving).  Key k of
+ * sequence b lives in row k % page_size of page block_table[b][k / page_size]
+ * of the page pools:
+ *   k_pages, v_pages [num_pages, page_size, Hkv, d] bf16, 16-byte aligned;
+ *   block_table: device int32 [B, max_blocks], row b lists the pages of
+ *            sequence b in key order (entries past its length are not read);
+ *   page_size: a positive multiple of 64 (the kernel's key tile), with
+ *            chunk / page_size + 2 <= 128 (pages of one split);
+ *   seqlens: device int32 [B], each in [0, max_blocks * page_size].
+ * The other arguments, the workspace (sized for max_seqlen = max_blocks *
+ * page_size) and the results are those of attn_fwd_splitkv.  A page index
+ * outside [0, num_pages) is replaced by page 0 for the read and reported as
+ * ATTN_ERR_DEVICE_ARG by attn_get_device_status.
+ */
+ATTN_API attn_status attn_fwd_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                                            const int* block_table, int max_blocks, int page_size,
+                                            int num_pages, const int* seqlens,
+                                            void* o, float* lse,
+                                            int B, int Hq, int Hkv, int d, float scale, int chunk,
+                                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Split-KV decode that allocates nothing, for callers that cannot call

@@ -92,6 +92,19 @@ def all_rows(B, Hq, Nq):
     return np.stack([b.ravel(), h.ravel(), i.ravel()], axis=1).astype(np.int32)
 
 
+def paged_to_contiguous(pages, block_table):
+    """The logical cache a paged one stands for: key k of sequence b is row
+    k % page_size of page block_table[b, k // page_size] (pyshine.com
+    flash-attention tour, "Why You Need This": paged KV cache).
+    pages [num_pages, page_size, H, d], block_table int [B, max_blocks] ->
+    [B, max_blocks * page_size, H, d]."""
+    bt = np.asarray(block_table, dtype=np.int64)
+    pages = np.asarray(pages) if not hasattr(pages, "numpy") else pages
+    gathered = pages[bt.reshape(-1)]                      # [B*max_blocks, page_size, H, d]
+    B, mb = bt.shape
+    return gathered.reshape((B, mb * gathered.shape[1]) + tuple(gathered.shape[2:]))
+
+
 def attn_fwd(q, k, v, causal, scale, kv_len=None, n_threads=None):
     """Full forward: O [B, Nq, Hq, d] float64 and LSE [B, Hq, Nq] float64."""
     qb = _bf16_bits(q)

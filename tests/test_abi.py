@@ -86,3 +86,26 @@ def test_splitkv_argument_checks(L):
     assert need == 2 * 8 * 2 * 128 * 4 + 2 * 8 * 2 * 4
     assert _splitkv(L, wsb=need - 1) == 7
     assert L.attn_splitkv_workspace_size(2, 8, 2048, 128, 1000) == 0
+
+
+def _paged(L, **kw):
+    a = dict(q=16, k=16, v=16, bt=16, mb=8, ps=256, npg=64, s=16, o=16, lse=16, B=2, Hq=8, Hkv=2, d=128,
+             scale=0.1, chunk=1024, ws=16, wsb=1 << 30)
+    a.update(kw)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.attn_fwd_splitkv_paged(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["bt"]), a["mb"], a["ps"], a["npg"],
+                                    vp(a["s"]), vp(a["o"]), vp(a["lse"]), a["B"], a["Hq"], a["Hkv"], a["d"],
+                                    a["scale"], a["chunk"], vp(a["ws"]), a["wsb"], None)
+
+
+def test_paged_splitkv_argument_checks(L):
+    assert _paged(L, bt=0) == 1               # no block table
+    assert _paged(L, ps=100) == 1             # page not a multiple of the 64-key tile
+    assert _paged(L, ps=0) == 1
+    assert _paged(L, mb=0) == 1
+    assert _paged(L, npg=0) == 1
+    assert _paged(L, ps=64, chunk=8192) == 2  # more pages per split than the kernel lists
+    assert _paged(L, bt=18) == 3              # misaligned block table
+    assert _paged(L, Hq=6, Hkv=4) == 1        # the checks of the contiguous call apply
+    need = L.attn_splitkv_workspace_size(2, 8, 8 * 256, 128, 1024)   # capacity max_blocks * page_size
+    assert _paged(L, wsb=need - 1) == 7

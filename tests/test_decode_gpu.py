@@ -77,6 +77,45 @@ def test_many_sequences(B):
     _check(q, k, v, L, 0.125, 64, "B%d" % B)
 
 
+def _check_paged(q, k, v, L, scale, chunk, page_size, what, seed=0):
+    """Paged decode against the oracle on the logical cache the pages stand for."""
+    kp, vp, bt = workloads.page_cache(k, v, page_size, seed=seed)
+    o, lse = _native.decode_paged(q.cuda(), kp.cuda(), vp.cuda(), bt.cuda(), L.cuda(), scale, chunk)
+    assert _native.attn_get_device_status() == 0
+    kc = oracle.paged_to_contiguous(kp, bt)
+    vc = oracle.paged_to_contiguous(vp, bt)
+    o_ref, lse_ref = oracle.attn_fwd(q, kc, vc, False, scale, kv_len=L.numpy())
+    return compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, what)
+
+
+@pytest.mark.parametrize("page_size,chunk", [(64, 1024), (256, 1024), (256, 256), (512, 1024), (1024, 256)])
+def test_paged_cache(page_size, chunk):
+    """Pages in a shuffled order, unused pages full of NaN, lengths that end
+    inside a page, on a page boundary, and at zero."""
+    lens = [3000, 1536, 1, 0, 700]
+    q, k, v, L = workloads.decode_inputs(len(lens), 8, 2, 3072, 128, 0, 0, seed=45, seqlens=lens)
+    _check_paged(q, k, v, L, 128 ** -0.5, chunk, page_size, "paged ps%d chunk%d" % (page_size, chunk), seed=page_size)
+
+
+def test_paged_cache_gqa_d64():
+    lens = [640, 1, 1024]
+    q, k, v, L = workloads.decode_inputs(len(lens), 12, 3, 1024, 64, 0, 0, seed=46, seqlens=lens)
+    _check_paged(q, k, v, L, 0.125, 512, 128, "paged gqa d64")
+
+
+def test_paged_bad_page_is_reported():
+    """A block-table entry outside the page pool reads page 0 instead and is
+    reported on the device; nothing faults."""
+    lens = [300, 200]
+    q, k, v, L = workloads.decode_inputs(2, 4, 2, 512, 128, 0, 0, seed=47, seqlens=lens)
+    kp, vp, bt = workloads.page_cache(k, v, 256, seed=3)
+    bt = bt.clone()
+    bt[1, 0] = kp.shape[0] + 5
+    _native.attn_get_device_status()  # clear
+    o, lse = _native.decode_paged(q.cuda(), kp.cuda(), vp.cuda(), bt.cuda(), L.cuda(), 0.1, 256)
+    assert _native.attn_get_device_status() == _native.ATTN_ERR_DEVICE_ARG
+
+
 def test_zero_length_sequence():
     lens = [0, 17]
     q, k, v, L = workloads.decode_inputs(2, 4, 2, 128, 128, 0, 0, seed=41, seqlens=lens)

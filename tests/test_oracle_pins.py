@@ -258,3 +258,26 @@ def test_nan_beyond_cache_length_is_never_read():
     o, lse = oracle.attn_fwd(q, k, v, False, 0.25, kv_len=L.numpy())
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     assert torch.isnan(k[1, 1:]).all()
+
+
+def test_paged_cache_definition_by_hand():
+    """Page table semantics on a hand example: key k of sequence b is row
+    k % page_size of page block_table[b, k // page_size]."""
+    pages = torch.arange(6, dtype=torch.float32).reshape(3, 2, 1, 1)   # page p holds 2p, 2p+1
+    bt = torch.tensor([[2, 0], [1, 2]], dtype=torch.int32)
+    got = oracle.paged_to_contiguous(pages, bt)[..., 0, 0]
+    assert got.tolist() == [[4.0, 5.0, 0.0, 1.0], [2.0, 3.0, 4.0, 5.0]]
+
+
+def test_paged_cache_round_trip():
+    """Scattering a cache into shuffled pages (the input generator) and
+    gathering it back (the oracle's definition) returns the cache."""
+    from exact_io_aware_14_gb300 import workloads as W
+    q, k, v, L = W.decode_inputs(3, 4, 2, 300, 64, 0, 0, seed=1, seqlens=[300, 17, 0])
+    for ps in (64, 256):
+        kp, vp, bt = W.page_cache(k, v, ps, seed=ps)
+        assert sorted(set(bt.reshape(-1).tolist())) == sorted(bt.reshape(-1).tolist())   # pages not shared
+        kc = oracle.paged_to_contiguous(kp, bt)[:, :300]
+        vc = oracle.paged_to_contiguous(vp, bt)[:, :300]
+        assert torch.equal(torch.nan_to_num(kc.float(), nan=7.0), torch.nan_to_num(k.float(), nan=7.0))
+        assert torch.equal(torch.nan_to_num(vc.float(), nan=7.0), torch.nan_to_num(v.float(), nan=7.0))
