@@ -56,6 +56,14 @@ def _bf16_bits(x):
     return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16))
 
 
+def _causal_code(causal):
+    """False/0: none; True/1: aligned top-left; 2: aligned bottom-right."""
+    c = int(causal)
+    if c not in (0, 1, 2):
+        raise ValueError("causal must be 0, 1 (top-left) or 2 (bottom-right)")
+    return c
+
+
 def attn_rows(q, k, v, rows, causal, scale, kv_len=None, n_threads=None):
     """O and LSE for the listed query rows.
 
@@ -79,7 +87,7 @@ def attn_rows(q, k, v, rows, causal, scale, kv_len=None, n_threads=None):
     rc = lib.oracle_attn_rows(
         qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
         B, Hq, Hkv, Nq, Nk, d,
-        None if kl is None else kl.ctypes.data, int(bool(causal)), float(scale),
+        None if kl is None else kl.ctypes.data, _causal_code(causal), float(scale),
         rows.ctypes.data, n, o.ctypes.data, lse.ctypes.data, nt)
     if rc != 0:
         raise ValueError("oracle_attn_rows failed with code %d" % rc)

@@ -21,9 +21,12 @@
  *                                       tour, "Why You Need This": K and V
  *                                       carry fewer heads, counts divide)
  *   L        = kv_len ? kv_len[b] : Nk
- *   visible(i, j) = (j < L) && (!causal || j <= i)   -- causal is aligned
- *                                       top-left: key j is seen by row i
- *                                       iff j <= i
+ *   visible(i, j) = (j < L) && (causal == 0 || j <= i + off)
+ *            causal 1: aligned top-left, off = 0 (key j is seen by row i
+ *                      iff j <= i);
+ *            causal 2: aligned bottom-right, off = L - Nq (the last query
+ *                      row sees every key; the pyshine.com flash-attention
+ *                      tour, "Why You Need This", names this alignment)
  *   s_j      = scale * sum_t q[i,t] * k[j,t]    (fp64; -inf if masked)
  *   m        = max_j s_j
  *   LSE      = m + ln(sum_j exp(s_j - m))       (natural log)
@@ -76,13 +79,14 @@ static void one_row(const oracle_job *J, int64_t r, double *s)
     const int group = J->Hq / J->Hkv;
     const int hkv = hq / group;
     const int L = J->kv_len ? J->kv_len[b] : J->Nk;
+    const int off = (J->causal == 2) ? L - J->Nq : 0;
     const uint16_t *qrow = J->q + (((int64_t)b * J->Nq + i) * J->Hq + hq) * d;
     double *orow = J->o + r * d;
 
     /* pass 1: every score of the row, -inf where masked, and the row max */
     double m = -INFINITY;
     for (int j = 0; j < J->Nk; ++j) {
-        int visible = (j < L) && (!J->causal || j <= i);
+        int visible = (j < L) && (J->causal == 0 || j <= i + off);
         if (!visible) {
             s[j] = -INFINITY;
             continue;
@@ -147,6 +151,8 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      double *o, double *lse, int n_threads)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0 || d <= 0 || Hq % Hkv != 0)
+        return -1;
+    if (causal < 0 || causal > 2)
         return -1;
     for (int64_t r = 0; r < n_rows; ++r) {
         const int32_t *t = rows + 3 * r;

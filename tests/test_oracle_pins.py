@@ -281,3 +281,50 @@ def test_paged_cache_round_trip():
         vc = oracle.paged_to_contiguous(vp, bt)[:, :300]
         assert torch.equal(torch.nan_to_num(kc.float(), nan=7.0), torch.nan_to_num(k.float(), nan=7.0))
         assert torch.equal(torch.nan_to_num(vc.float(), nan=7.0), torch.nan_to_num(v.float(), nan=7.0))
+
+
+@pytest.mark.parametrize("Nq,Nk", [(7, 29), (29, 7), (16, 16), (1, 50)])
+def test_bottom_right_causal_matches_sdpa_with_its_mask(Nq, Nk):
+    """causal=2 (aligned bottom-right: row i sees keys j <= i + Nk - Nq)
+    against torch's fp64 SDPA with that boolean mask written out; rows that
+    see no key are O = 0, LSE = -inf."""
+    B, Hq, Hkv, d = 2, 4, 2, 16
+    q, k, v = _rand(B, Hq, Hkv, Nq, Nk, d, seed=21)
+    o, lse = oracle.attn_fwd(q, k, v, 2, 0.25)
+    mask = torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+    seen = mask.any(dim=1)
+    tq, tk, tv = (x.double().permute(0, 2, 1, 3) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk, tv, attn_mask=mask, scale=0.25, enable_gqa=True).permute(0, 2, 1, 3).numpy()
+    np.testing.assert_allclose(o[:, seen.numpy()], ref[:, seen.numpy()], rtol=0, atol=1e-12)
+    assert (o[:, ~seen.numpy()] == 0).all()
+    assert np.isneginf(lse[:, :, ~seen.numpy()]).all()
+
+
+def test_bottom_right_causal_special_cases():
+    """Nq == Nk: bottom-right is top-left; Nq == 1: the one row sees every key."""
+    q, k, v = _rand(1, 2, 2, 24, 24, 16, seed=22)
+    a = oracle.attn_fwd(q, k, v, 1, 0.3)
+    b = oracle.attn_fwd(q, k, v, 2, 0.3)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    q1, k1, v1 = _rand(1, 2, 2, 1, 37, 16, seed=23)
+    c = oracle.attn_fwd(q1, k1, v1, 2, 0.3)
+    e = oracle.attn_fwd(q1, k1, v1, False, 0.3)
+    assert np.array_equal(c[0], e[0]) and np.array_equal(c[1], e[1])
+    with pytest.raises(ValueError):
+        oracle.attn_fwd(q, k, v, 3, 0.3)
+
+
+def test_bottom_right_with_cache_lengths_is_prefill_against_a_cache():
+    """With kv_len, bottom-right puts query row i at cache position
+    L_b - Nq + i: the same as the rows of one causal pass over the whole
+    cache (top-left, Nq = Nk = L_b) that hold the last Nq positions."""
+    B, Hq, Hkv, Nq, S, d = 2, 4, 2, 5, 30, 16
+    q, k, v = _rand(B, Hq, Hkv, S, S, d, seed=24)
+    kv_len = [30, 12]
+    for b, L in enumerate(kv_len):
+        o_full, l_full = oracle.attn_fwd(q[b:b + 1, :L], k[b:b + 1, :L], v[b:b + 1, :L], True, 0.2)
+        qs = q[b:b + 1, L - Nq:L].contiguous()
+        o_tail, l_tail = oracle.attn_fwd(qs, k[b:b + 1], v[b:b + 1], 2, 0.2, kv_len=[L])
+        np.testing.assert_allclose(o_tail, o_full[:, L - Nq:L], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l_tail, l_full[:, :, L - Nq:L], rtol=0, atol=1e-13)
