@@ -94,7 +94,7 @@ def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
     if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("lse must be a contiguous CUDA fp32 tensor of shape %s" % ((B, Hq, Nq),))
     return lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                          int(bool(causal)), float(scale), _stream_handle(stream))
+                          int(causal), float(scale), _stream_handle(stream))
 
 
 def attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk):

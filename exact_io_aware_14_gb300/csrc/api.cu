@@ -73,7 +73,7 @@ const char* attn_status_string(attn_status s) {
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, int causal, float scale, void* stream) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || (Hq % Hkv) != 0) return ATTN_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   // 32-bit TMA coordinates and grid: keep rows and tiles well inside int range
@@ -104,7 +104,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.Nq = Nq;
   p.Nk = Nk;
   p.d = d;
-  p.causal = causal;
+  p.causal = causal != 0;
+  p.causal_off = causal == 2 ? Nk - Nq : 0;  // bottom-right: the last row sees every key
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   return attn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

@@ -17,6 +17,7 @@ struct PrefillParams {
   void* o;
   float* lse;
   int B, Hq, Hkv, Nq, Nk, d, causal;
+  int causal_off;    // causal: key j is visible to row i iff j <= i + causal_off
   float scale_log2;  // scale * log2(e)
 };
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);

@@ -175,7 +175,7 @@ struct Unit {
   int b, hkv, n_kt;
   TileInfo ti[2];
 };
-__device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
+__device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal, int coff,
                                             int pair_heads, int units_per_bh) {
   Unit u;
   const int hslots = pair_heads ? Hq / 2 : Hq;
@@ -197,7 +197,7 @@ __device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int N
   u.hkv = u.ti[0].hq / (Hq / Hkv);  // both heads of a pair share the KV head
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int kend = causal ? min(Nk, u.ti[t].row0 + BM) : Nk;
+    const int kend = causal ? max(0, min(Nk, u.ti[t].row0 + BM + coff)) : Nk;
     u.ti[t].n_kt = (u.ti[t].row0 < Nq) ? (kend + BN - 1) / BN : 0;
   }
   u.n_kt = max(u.ti[0].n_kt, u.ti[1].n_kt);
@@ -220,7 +220,7 @@ template <int D, bool kNeg>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
-                       float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
+                       float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal, int coff,
                        float scale_log2, int pair_heads, int units_per_bh, int total_units) {
   using L = Layout<D>;
   constexpr int NS = L::kSlots;
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, pair_heads, units_per_bh);
+        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, coff, pair_heads, units_per_bh);
         for (int t = 0; t < 2; ++t) {
           // Q_t of the previous unit must have been read by its last QK^T
           if (uc >= 1 && !wait_one(bar_qfree + t, (uc - 1) & 1, abort_flag, 1)) { ok = false; break; }
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, pair_heads, units_per_bh);
+        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, coff, pair_heads, units_per_bh);
         const int n_kt = u.n_kt;
         for (int t = 0; t < 2 && ok; ++t) {
           ok = wait_one(bar_qfull + t, uc & 1, abort_flag, 3);
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
       const int U = unit_of_round(rnd, total_units);
       if (U < 0) continue;
-      const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, pair_heads, units_per_bh);
+      const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, coff, pair_heads, units_per_bh);
       const TileInfo me = t ? u.ti[1] : u.ti[0];
       const int grow = me.row0 + r;
       const int my_kt = me.n_kt;
@@ -489,11 +489,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_all(bar_sfull + t, (kc + j) & 1, abort_flag, 7)) { ok = false; break; }
         tc_fence_after();
         const int kbase = j * BN;
-        const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0);
+        const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0 + coff);
         int lim = BN;  // columns [lim, BN) of this tile are masked for this row
         if (masked) {
           lim = Nk - kbase;
-          if (causal) lim = min(lim, grow - kbase + 1);
+          if (causal) lim = min(lim, grow + coff - kbase + 1);
         }
         const float mt = masked ? score_tile_max<true, kNeg>(tS, lim) : score_tile_max<false, kNeg>(tS, lim);
         // move the reference only on the first visible scores or when the tile
@@ -608,7 +608,7 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, L::kAlloc, stream>>>(p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B,
-                                              p.Hq, p.Hkv, p.Nq, p.Nk, p.causal, p.scale_log2, pair_heads,
+                                              p.Hq, p.Hkv, p.Nq, p.Nk, p.causal, p.causal_off, p.scale_log2, pair_heads,
                                               units_per_bh, static_cast<int>(total));
   return cudaGetLastError();
 }

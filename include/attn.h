@@ -63,10 +63,19 @@ typedef enum {
   ATTN_ERR_WORKSPACE = 7     /* workspace missing or smaller than required */
 } attn_status;
 
+#define ATTN_CAUSAL_NONE 0
+#define ATTN_CAUSAL_TOP_LEFT 1
+#define ATTN_CAUSAL_BOTTOM_RIGHT 2
+
 /*
  * Prefill / training-shape forward.
  *   q [B,Nq,Hq,d], k and v [B,Nk,Hkv,d] bf16 in; o [B,Nq,Hq,d] bf16 and
- *   lse [B,Hq,Nq] fp32 out.  causal: 0 or 1 (top-left aligned).
+ *   lse [B,Hq,Nq] fp32 out.
+ *   causal: ATTN_CAUSAL_NONE (0); ATTN_CAUSAL_TOP_LEFT (1): key j is seen
+ *            by row i iff j <= i; ATTN_CAUSAL_BOTTOM_RIGHT (2): iff
+ *            j <= i + Nk - Nq, so the last query row sees every key (the
+ *            alignment the pyshine.com flash-attention tour names; with
+ *            Nq > Nk the first Nq - Nk rows see none: O = 0, LSE = -inf).
  *   scale: finite softmax scale applied to Q K^T (1/sqrt(d) usually).
  * Tiled over 128-row query tiles and 128-key K/V tiles: TMA loads into
  * shared memory, tcgen05 MMAs accumulate S = Q K^T and O += P V in Tensor

@@ -53,7 +53,8 @@ def test_attn_fwd_argument_checks(L):
     assert _fwd(L, Hq=3, Hkv=2) == 1          # heads do not divide
     assert _fwd(L, B=0) == 1
     assert _fwd(L, Nq=-1) == 1
-    assert _fwd(L, causal=2) == 1
+    assert _fwd(L, causal=3) == 1             # 0 none, 1 top-left, 2 bottom-right
+    assert _fwd(L, causal=-1) == 1
     assert _fwd(L, scale=float("nan")) == 1
     assert _fwd(L, scale=float("inf")) == 1
     assert _fwd(L, d=96) == 2                 # not built

@@ -69,6 +69,18 @@ def test_small_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
     _full_check(q, k, v, causal, 1 / math.sqrt(d), "B%d Hq%d Hkv%d Nq%d Nk%d d%d c%d" % (B, Hq, Hkv, Nq, Nk, d, causal))
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d", [
+    (1, 4, 2, 200, 333, 64),      # Nq < Nk: every row sees the first Nk - Nq keys
+    (1, 3, 1, 390, 130, 128),     # Nq > Nk: the first 260 rows see nothing
+    (2, 4, 4, 130, 1000, 128),    # a short query block at the end of a long key range
+    (2, 32, 8, 300, 700, 128),    # GQA head pairs, several units per CTA
+    (1, 2, 2, 257, 257, 128),     # Nq == Nk: the same as top-left
+])
+def test_bottom_right_causal(B, Hq, Hkv, Nq, Nk, d):
+    q, k, v = workloads.prefill_inputs(B, Hq, Hkv, Nq, Nk, d, seed=200 + Nq + Nk)
+    _full_check(q, k, v, 2, 1 / math.sqrt(d), "bottom-right B%d Hq%d Hkv%d Nq%d Nk%d d%d" % (B, Hq, Hkv, Nq, Nk, d))
+
+
 @pytest.mark.parametrize("scale", [-0.09, 0.0, 0.5])
 def test_negative_zero_and_large_scale(scale):
     """A negative scale runs the sign-flipped kernel variant; scale 0 gives
