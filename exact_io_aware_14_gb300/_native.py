@@ -46,6 +46,8 @@ def lib():
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.attn_fwd.restype = i
         L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        L.attn_fwd_kvcache.restype = i
+        L.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, f, vp]
         L.attn_splitkv_workspace_size.restype = sz
         L.attn_splitkv_workspace_size.argtypes = [i, i, i, i, i]
         L.attn_fwd_splitkv.restype = i
@@ -95,6 +97,34 @@ def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
         raise ValueError("lse must be a contiguous CUDA fp32 tensor of shape %s" % ((B, Hq, Nq),))
     return lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                           int(causal), float(scale), _stream_handle(stream))
+
+
+def attn_fwd_kvcache(q, k_cache, v_cache, seqlens, o, lse, causal, scale, stream=None):
+    """Same contract as the C call: q, o [B,Nq,Hq,d]; caches [B,max_seqlen,Hkv,d];
+    seqlens int32 [B] on the device; lse [B,Hq,Nq].  Returns the status."""
+    B, Nq, Hq, d = q.shape
+    max_seqlen, Hkv = k_cache.shape[1], k_cache.shape[2]
+    _check_bf16("q", q, (B, Nq, Hq, d))
+    _check_bf16("k_cache", k_cache, (B, max_seqlen, Hkv, d))
+    _check_bf16("v_cache", v_cache, (B, max_seqlen, Hkv, d))
+    _check_bf16("o", o, (B, Nq, Hq, d))
+    if seqlens.dtype != torch.int32 or not seqlens.is_cuda or tuple(seqlens.shape) != (B,):
+        raise ValueError("seqlens must be a CUDA int32 tensor of shape (%d,)" % B)
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse must be a contiguous CUDA fp32 tensor of shape %s" % ((B, Hq, Nq),))
+    return lib().attn_fwd_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), max_seqlen, _ptr(o),
+                                  _ptr(lse), B, Hq, Hkv, Nq, d, int(causal), float(scale), _stream_handle(stream))
+
+
+def forward_kvcache(q, k_cache, v_cache, seqlens, causal, scale, stream=None):
+    """Allocates O and LSE and runs attn_fwd_kvcache. Returns (o, lse)."""
+    B, Nq, Hq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    rc = attn_fwd_kvcache(q, k_cache, v_cache, seqlens, o, lse, causal, scale, stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_kvcache")
+    return o, lse
 
 
 def attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk):

@@ -104,8 +104,43 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.Nq = Nq;
   p.Nk = Nk;
   p.d = d;
-  p.causal = causal != 0;
-  p.causal_off = causal == 2 ? Nk - Nq : 0;  // bottom-right: the last row sees every key
+  p.causal = causal;
+  p.seqlens = nullptr;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
+  return attn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+attn_status attn_fwd_kvcache(const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+                             int max_seqlen, void* o, float* lse, int B, int Hq, int Hkv, int Nq, int d, int causal,
+                             float scale, void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || max_seqlen < 1 || (Hq % Hkv) != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(Nq) + 127 > 0x7fffffffLL || static_cast<long long>(max_seqlen) + 127 > 0x7fffffffLL)
+    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>((Nq + 127) / 128) * B * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (Nq == 0) return ATTN_OK;
+  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+    return ATTN_ERR_MISALIGNED;
+
+  attn::PrefillParams p;
+  std::memset(&p, 0, sizeof p);
+  if (!make_map(&p.tm_q, q, B, Nq, Hq, d, 128) || !make_map(&p.tm_k, k_cache, B, max_seqlen, Hkv, d, 128) ||
+      !make_map(&p.tm_v, v_cache, B, max_seqlen, Hkv, d, 128))
+    return ATTN_ERR_LAUNCH;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nk = max_seqlen;
+  p.d = d;
+  p.causal = causal;
+  p.seqlens = seqlens;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   return attn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }

@@ -16,9 +16,10 @@ struct PrefillParams {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps {d, H, N, B}, box {64, 1, 128, 1}, 128-B swizzle
   void* o;
   float* lse;
-  int B, Hq, Hkv, Nq, Nk, d, causal;
-  int causal_off;    // causal: key j is visible to row i iff j <= i + causal_off
-  float scale_log2;  // scale * log2(e)
+  int B, Hq, Hkv, Nq, Nk, d;
+  int causal;            // 0 none, 1 aligned top-left, 2 aligned bottom-right
+  const int* seqlens;    // null, or keys per sequence (cache lengths <= Nk) on the device
+  float scale_log2;      // scale * log2(e)
 };
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 

@@ -57,7 +57,7 @@ struct Layout {
   static constexpr int kOffQ = 0;  // Q_0, Q_1
   static constexpr int kOffRing = kOffQ + 2 * kTile;
   static constexpr int kOffBar = kOffRing + kSlots * kTile;
-  static constexpr int kNumBars = 2 * kSlots + 6 * 2;
+  static constexpr int kNumBars = 2 * kSlots + 6 * 2 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -170,13 +170,16 @@ __device__ __forceinline__ float score_tile_exp(uint32_t tS, int lim, float c, f
 
 // Work unit U -> (batch, KV head, the two query tiles).  Units are numbered
 // (u_rev, head slot, batch) with u_rev slowest, so causal units come longest
-// first.
+// first.  Keys of the unit's sequence: nk (Nk, or its cache length when
+// seqlens is given); causal mode 1 aligns top-left, 2 bottom-right (key j
+// visible to row i iff j <= i + coff).
 struct Unit {
   int b, hkv, n_kt;
+  int nk, coff;
   TileInfo ti[2];
 };
-__device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal, int coff,
-                                            int pair_heads, int units_per_bh) {
+__device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
+                                            const int* __restrict__ seqlens, int pair_heads, int units_per_bh) {
   Unit u;
   const int hslots = pair_heads ? Hq / 2 : Hq;
   const int bh_count = B * hslots;
@@ -195,9 +198,11 @@ __device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int N
     u.ti[1].row0 = (2 * unit + 1) * BM;
   }
   u.hkv = u.ti[0].hq / (Hq / Hkv);  // both heads of a pair share the KV head
+  u.nk = seqlens ? min(max(seqlens[u.b], 0), Nk) : Nk;
+  u.coff = (causal == 2) ? u.nk - Nq : 0;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int kend = causal ? max(0, min(Nk, u.ti[t].row0 + BM + coff)) : Nk;
+    const int kend = causal ? max(0, min(u.nk, u.ti[t].row0 + BM + u.coff)) : u.nk;
     u.ti[t].n_kt = (u.ti[t].row0 < Nq) ? (kend + BN - 1) / BN : 0;
   }
   u.n_kt = max(u.ti[0].n_kt, u.ti[1].n_kt);
@@ -216,14 +221,18 @@ __device__ __forceinline__ int unit_of_round(int r, int total_units) {
 // Barrier phases run on across units: per-unit barriers by the unit count
 // `uc`, score / P barriers by the running key-tile count of each query tile,
 // ring slots by the running item count.
-template <int D, bool kNeg>
+// kCache: keys per sequence come from seqlens (attn_fwd_kvcache); otherwise
+// every sequence has Nk keys and seqlens is not read.
+template <int D, bool kNeg, bool kCache>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
-                       float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal, int coff,
+                       float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
+                       const int* __restrict__ seqlens,
                        float scale_log2, int pair_heads, int units_per_bh, int total_units) {
   using L = Layout<D>;
   constexpr int NS = L::kSlots;
+  const int* const lens = kCache ? seqlens : nullptr;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -236,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_qfull = bar_odone + 2;    // [2] Q_t loaded
   uint64_t* bar_qfree = bar_qfull + 2;    // [2] last QK^T of the unit read Q_t
   uint64_t* bar_ofree = bar_qfree + 2;    // [2] epilogue read O_t out of TMEM (4 softmax warps)
+  uint64_t* bar_vfix = bar_ofree + 2;     // last V tile of a cache row landed (producer only)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
@@ -255,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_qfree + t, 1);
       mbar_init(bar_ofree + t, 4);
     }
+    mbar_init(bar_vfix, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -276,13 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      uint32_t item_base = 0;
+      uint32_t item_base = 0, vfix_uses = 0;
       int uc = 0;
       bool ok = true;
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, coff, pair_heads, units_per_bh);
+        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, lens, pair_heads, units_per_bh);
+        if (kCache && (lens[u.b] < 0 || lens[u.b] > Nk) && u.ti[0].hq == 0) record(11, kDevBadSeqlen);
         for (int t = 0; t < 2; ++t) {
           // Q_t of the previous unit must have been read by its last QK^T
           if (uc >= 1 && !wait_one(bar_qfree + t, (uc - 1) & 1, abort_flag, 1)) { ok = false; break; }
@@ -298,10 +310,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           // item -> (K or V, key tile), the inverse of k_item / v_item
           const bool is_v = (item == 2 * u.n_kt - 1) || (item > 0 && (item & 1) == 0);
           const int kt = (item == 2 * u.n_kt - 1) ? u.n_kt - 1 : (is_v ? item / 2 - 1 : (item + 1) / 2);
-          mbar_arrive_expect_tx(bar_full + slot, L::kTile);
+          // A cache's last V tile may run past the cache length into rows that
+          // hold anything, NaN included (and P = 0 times NaN is not 0): it is
+          // loaded against a private barrier and those rows are cleared before
+          // the MMA thread is told the tile is there.
+          const int valid = u.nk - kt * BN;
+          const bool fix = kCache && is_v && valid < BN;
+          uint64_t* done = fix ? bar_vfix : bar_full + slot;
+          mbar_arrive_expect_tx(done, L::kTile);
           for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, bar_full + slot, h * 64,
-                        u.hkv, kt * BN, u.b);
+            tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, done, h * 64, u.hkv, kt * BN,
+                        u.b);
+          if (fix) {
+            if (!wait_one(bar_vfix, vfix_uses & 1, abort_flag, 12)) { ok = false; break; }
+            ++vfix_uses;
+            for (int h = 0; h < D / 64; ++h) {
+              uint8_t* base = sRing + slot * L::kTile + h * L::kHalf;
+              for (int off = max(valid, 0) * 128; off < BN * 128; off += 16)
+                *reinterpret_cast<uint4*>(base + off) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // the generic stores before the tensor core's reads
+            mbar_arrive(bar_full + slot);
+          }
         }
         item_base += 2 * u.n_kt;
         ++uc;
@@ -324,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, coff, pair_heads, units_per_bh);
+        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, lens, pair_heads, units_per_bh);
         const int n_kt = u.n_kt;
         for (int t = 0; t < 2 && ok; ++t) {
           ok = wait_one(bar_qfull + t, uc & 1, abort_flag, 3);
@@ -479,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
       const int U = unit_of_round(rnd, total_units);
       if (U < 0) continue;
-      const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, coff, pair_heads, units_per_bh);
+      const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, lens, pair_heads, units_per_bh);
       const TileInfo me = t ? u.ti[1] : u.ti[0];
       const int grow = me.row0 + r;
       const int my_kt = me.n_kt;
@@ -489,11 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_all(bar_sfull + t, (kc + j) & 1, abort_flag, 7)) { ok = false; break; }
         tc_fence_after();
         const int kbase = j * BN;
-        const bool masked = (kbase + BN > Nk) || (causal && kbase + BN - 1 > me.row0 + coff);
+        const bool masked = (kbase + BN > u.nk) || (causal && kbase + BN - 1 > me.row0 + u.coff);
         int lim = BN;  // columns [lim, BN) of this tile are masked for this row
         if (masked) {
-          lim = Nk - kbase;
-          if (causal) lim = min(lim, grow + coff - kbase + 1);
+          lim = u.nk - kbase;
+          if (causal) lim = min(lim, grow + u.coff - kbase + 1);
         }
         const float mt = masked ? score_tile_max<true, kNeg>(tS, lim) : score_tile_max<false, kNeg>(tS, lim);
         // move the reference only on the first visible scores or when the tile
@@ -604,11 +634,12 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(total < n_sm ? total : n_sm);  // one persistent CTA per SM
-  auto kern = (p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true> : prefill_fwd_kernel<D, false>;
+  auto kern = p.seqlens ? ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, true> : prefill_fwd_kernel<D, false, true>)
+                        : ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, false> : prefill_fwd_kernel<D, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, L::kAlloc, stream>>>(p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B,
-                                              p.Hq, p.Hkv, p.Nq, p.Nk, p.causal, p.causal_off, p.scale_log2, pair_heads,
+                                              p.Hq, p.Hkv, p.Nq, p.Nk, p.causal, p.seqlens, p.scale_log2, pair_heads,
                                               units_per_bh, static_cast<int>(total));
   return cudaGetLastError();
 }

@@ -93,6 +93,27 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
                      int causal, float scale, void* stream);
 
 /*
+ * The same forward against a KV cache with a length per sequence: a block
+ * of Nq new query rows (a chunk of a prompt, or several decode tokens)
+ * attends to the first seqlens[b] keys of sequence b (pyshine.com
+ * flash-attention tour, "Why You Need This": prefill and decode against a
+ * KV cache with per-sequence lengths).
+ *   q [B,Nq,Hq,d] bf16; k_cache, v_cache [B,max_seqlen,Hkv,d] bf16;
+ *   seqlens: device int32 [B], each in [0, max_seqlen]; keys at or past
+ *            seqlens[b] are never read into the result, whatever they hold;
+ *   o [B,Nq,Hq,d] bf16, lse [B,Hq,Nq] fp32 out;
+ *   causal: as for attn_fwd, with Nk = seqlens[b]: ATTN_CAUSAL_BOTTOM_RIGHT
+ *            puts query row i at cache position seqlens[b] - Nq + i (the
+ *            new rows are the last Nq keys of the cache).
+ * Constraints and errors are those of attn_fwd; a seqlens entry outside
+ * [0, max_seqlen] is clamped and reported as ATTN_ERR_DEVICE_ARG by
+ * attn_get_device_status.
+ */
+ATTN_API attn_status attn_fwd_kvcache(const void* q, const void* k_cache, const void* v_cache,
+                             const int* seqlens, int max_seqlen, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Nq, int d, int causal, float scale, void* stream);
+
+/*
  * Bytes of workspace attn_fwd_splitkv needs: fp32 partial outputs and
  * partial LSEs for ceil(max_seqlen / chunk) splits of every (b, hq).
  * Returns 0 for invalid arguments.

@@ -110,3 +110,22 @@ def test_paged_splitkv_argument_checks(L):
     assert _paged(L, Hq=6, Hkv=4) == 1        # the checks of the contiguous call apply
     need = L.attn_splitkv_workspace_size(2, 8, 8 * 256, 128, 1024)   # capacity max_blocks * page_size
     assert _paged(L, wsb=need - 1) == 7
+
+
+def _kvc(L, **kw):
+    a = dict(q=16, k=16, v=16, s=16, S=512, o=16, lse=16, B=2, Hq=8, Hkv=2, Nq=40, d=128, causal=2, scale=0.1)
+    a.update(kw)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.attn_fwd_kvcache(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["s"]), a["S"], vp(a["o"]), vp(a["lse"]),
+                              a["B"], a["Hq"], a["Hkv"], a["Nq"], a["d"], a["causal"], a["scale"], None)
+
+
+def test_kvcache_argument_checks(L):
+    assert _kvc(L, causal=3) == 1
+    assert _kvc(L, S=0) == 1
+    assert _kvc(L, Hq=6, Hkv=4) == 1
+    assert _kvc(L, s=0) == 1                  # no cache lengths
+    assert _kvc(L, d=80) == 2
+    assert _kvc(L, k=24) == 3
+    assert _kvc(L, s=18) == 3                 # misaligned lengths
+    assert _kvc(L, Nq=0) == 0                 # nothing to do
