@@ -33,7 +33,7 @@ def _load():
         lib.oracle_attn_rows.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_void_p, ctypes.c_int, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
             ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
         ]
@@ -64,11 +64,21 @@ def _causal_code(causal):
     return c
 
 
-def attn_rows(q, k, v, rows, causal, scale, kv_len=None, n_threads=None):
+def _window(window):
+    """None, or (left, right): row i (at key position i + L - Nq) sees keys
+    from position - left to position + right; a negative side is unbounded."""
+    if window is None:
+        return -1, -1
+    wl, wr = (int(x) for x in window)
+    return wl, wr
+
+
+def attn_rows(q, k, v, rows, causal, scale, kv_len=None, n_threads=None, window=None):
     """O and LSE for the listed query rows.
 
     q: [B, Nq, Hq, d] bf16; k, v: [B, Nk, Hkv, d] bf16 (Nk = allocated length);
-    rows: int array [n, 3] of (b, hq, i); kv_len: optional int32 [B] valid keys.
+    rows: int array [n, 3] of (b, hq, i); kv_len: optional int32 [B] valid keys;
+    window: optional local window (left, right), see ``_window``.
     Returns (o [n, d] float64, lse [n] float64).
     """
     lib = _load()
@@ -87,7 +97,7 @@ def attn_rows(q, k, v, rows, causal, scale, kv_len=None, n_threads=None):
     rc = lib.oracle_attn_rows(
         qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
         B, Hq, Hkv, Nq, Nk, d,
-        None if kl is None else kl.ctypes.data, _causal_code(causal), float(scale),
+        None if kl is None else kl.ctypes.data, _causal_code(causal), *_window(window), float(scale),
         rows.ctypes.data, n, o.ctypes.data, lse.ctypes.data, nt)
     if rc != 0:
         raise ValueError("oracle_attn_rows failed with code %d" % rc)
@@ -113,9 +123,9 @@ def paged_to_contiguous(pages, block_table):
     return gathered.reshape((B, mb * gathered.shape[1]) + tuple(gathered.shape[2:]))
 
 
-def attn_fwd(q, k, v, causal, scale, kv_len=None, n_threads=None):
+def attn_fwd(q, k, v, causal, scale, kv_len=None, n_threads=None, window=None):
     """Full forward: O [B, Nq, Hq, d] float64 and LSE [B, Hq, Nq] float64."""
     qb = _bf16_bits(q)
     B, Nq, Hq, d = qb.shape
-    o, lse = attn_rows(qb, k, v, all_rows(B, Hq, Nq), causal, scale, kv_len, n_threads)
+    o, lse = attn_rows(qb, k, v, all_rows(B, Hq, Nq), causal, scale, kv_len, n_threads, window)
     return o.reshape(B, Nq, Hq, d), lse.reshape(B, Nq, Hq).transpose(0, 2, 1).copy()

@@ -27,6 +27,17 @@
  *            causal 2: aligned bottom-right, off = L - Nq (the last query
  *                      row sees every key; the pyshine.com flash-attention
  *                      tour, "Why You Need This", names this alignment)
+ *            && (wl < 0 || j >= i + (L - Nq) - wl)
+ *            && (wr < 0 || j <= i + (L - Nq) + wr)
+ *                      local (sliding-window) attention, window (wl, wr):
+ *                      row i sees keys no more than wl positions before it
+ *                      and wr after it ("FlashAttention: Part 2", section
+ *                      3.2: local attention keeps i -> j only for
+ *                      |i - j| <= w; the pyshine.com tour, "From Install
+ *                      to Causal Attention", passes the window as a
+ *                      (left, right) pair next to causal).  Positions are
+ *                      aligned bottom-right, as for causal 2; a negative
+ *                      side is unbounded.
  *   s_j      = scale * sum_t q[i,t] * k[j,t]    (fp64; -inf if masked)
  *   m        = max_j s_j
  *   LSE      = m + ln(sum_j exp(s_j - m))       (natural log)
@@ -60,6 +71,7 @@ typedef struct {
     int B, Hq, Hkv, Nq, Nk, d;
     const int32_t *kv_len;
     int causal;
+    int wl, wr;
     double scale;
     const int32_t *rows; /* triples (b, hq, i) */
     int64_t n_rows;
@@ -80,13 +92,15 @@ static void one_row(const oracle_job *J, int64_t r, double *s)
     const int hkv = hq / group;
     const int L = J->kv_len ? J->kv_len[b] : J->Nk;
     const int off = (J->causal == 2) ? L - J->Nq : 0;
+    const int64_t pos = (int64_t)i + L - J->Nq; /* row i's key position, bottom-right */
     const uint16_t *qrow = J->q + (((int64_t)b * J->Nq + i) * J->Hq + hq) * d;
     double *orow = J->o + r * d;
 
     /* pass 1: every score of the row, -inf where masked, and the row max */
     double m = -INFINITY;
     for (int j = 0; j < J->Nk; ++j) {
-        int visible = (j < L) && (J->causal == 0 || j <= i + off);
+        int visible = (j < L) && (J->causal == 0 || j <= i + off) &&
+                      (J->wl < 0 || j >= pos - J->wl) && (J->wr < 0 || j <= pos + J->wr);
         if (!visible) {
             s[j] = -INFINITY;
             continue;
@@ -142,11 +156,13 @@ static void *worker(void *arg)
 
 /*
  * Computes the rows listed in `rows` (n_rows triples b, hq, i).
+ * window_left / window_right: the local window (negative: unbounded side).
  * Returns 0 on success, -1 on a bad argument, -2 on out-of-memory.
  */
 int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      int B, int Hq, int Hkv, int Nq, int Nk, int d,
-                     const int32_t *kv_len, int causal, double scale,
+                     const int32_t *kv_len, int causal, int window_left, int window_right,
+                     double scale,
                      const int32_t *rows, int64_t n_rows,
                      double *o, double *lse, int n_threads)
 {
@@ -175,7 +191,7 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     }
     int started = 0;
     for (int t = 0; t < n_threads; ++t) {
-        oracle_job J = {q, k, v, B, Hq, Hkv, Nq, Nk, d, kv_len, causal, scale,
+        oracle_job J = {q, k, v, B, Hq, Hkv, Nq, Nk, d, kv_len, causal, window_left, window_right, scale,
                         rows, n_rows, o, lse, n_threads, t, 0};
         jobs[t] = J;
     }

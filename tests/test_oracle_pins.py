@@ -328,3 +328,111 @@ def test_bottom_right_with_cache_lengths_is_prefill_against_a_cache():
         o_tail, l_tail = oracle.attn_fwd(qs, k[b:b + 1], v[b:b + 1], 2, 0.2, kv_len=[L])
         np.testing.assert_allclose(o_tail, o_full[:, L - Nq:L], rtol=0, atol=1e-13)
         np.testing.assert_allclose(l_tail, l_full[:, :, L - Nq:L], rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- local window
+# "FlashAttention: Part 2", section 3.2: local attention keeps i -> j only for
+# |i - j| <= w; the window is given as (left, right), positions aligned
+# bottom-right (row i at key position i + L - Nq), a negative side unbounded.
+
+def _band(Nq, Nk, wl, wr):
+    """Boolean [Nq, Nk] mask of the window, written out with torch."""
+    pos = torch.arange(Nq)[:, None] + (Nk - Nq)
+    j = torch.arange(Nk)[None, :]
+    m = torch.ones(Nq, Nk, dtype=torch.bool)
+    if wl >= 0:
+        m &= j >= pos - wl
+    if wr >= 0:
+        m &= j <= pos + wr
+    return m
+
+
+@pytest.mark.parametrize("Nq,Nk,wl,wr", [(16, 16, 3, 3), (16, 16, 2, 5), (9, 31, 4, 0), (31, 9, 6, 2),
+                                         (12, 40, -1, 3), (12, 40, 7, -1), (20, 20, 0, -1)])
+def test_window_matches_sdpa_with_its_band_mask(Nq, Nk, wl, wr):
+    """torch's fp64 CPU SDPA with the band |i - j| <= w (one bound per side)
+    as an explicit boolean mask; rows whose band holds no key: O = 0, LSE = -inf."""
+    B, Hq, Hkv, d = 2, 4, 2, 16
+    q, k, v = _rand(B, Hq, Hkv, Nq, Nk, d, seed=31 + Nq + wl)
+    o, lse = oracle.attn_fwd(q, k, v, 0, 0.25, window=(wl, wr))
+    mask = _band(Nq, Nk, wl, wr)
+    seen = mask.any(dim=1).numpy()
+    tq, tk, tv = (x.double().permute(0, 2, 1, 3) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk, tv, attn_mask=mask, scale=0.25, enable_gqa=True).permute(0, 2, 1, 3).numpy()
+    np.testing.assert_allclose(o[:, seen], ref[:, seen], rtol=0, atol=1e-12)
+    assert (o[:, ~seen] == 0).all() and np.isneginf(lse[:, :, ~seen]).all()
+
+
+def test_window_zero_is_the_diagonal():
+    """Window (0, 0), Nq == Nk: row i sees key i alone, so O_i = v_i exactly
+    and LSE_i is its one score."""
+    q, k, v = _rand(1, 2, 2, 20, 20, 16, seed=32)
+    o, lse = oracle.attn_fwd(q, k, v, 0, 0.4, window=(0, 0))
+    qd, kd = q.double().numpy(), k.double().numpy()
+    assert np.array_equal(o, v.double().numpy())
+    s = 0.4 * np.einsum("bihd,bihd->bhi", qd, kd)
+    np.testing.assert_allclose(lse, s, rtol=0, atol=1e-13)
+
+
+def test_window_one_left_is_a_two_key_softmax():
+    """Window (1, 0): row i >= 1 sees keys i-1 and i, weights
+    sigma(s_i - s_{i-1}) on v_i; row 0 sees key 0 alone."""
+    q, k, v = _rand(1, 1, 1, 15, 15, 8, seed=33)
+    o, lse = oracle.attn_fwd(q, k, v, 0, 0.5, window=(1, 0))
+    qd, kd, vd = (x.double().numpy()[0, :, 0] for x in (q, k, v))
+    s = 0.5 * np.einsum("id,jd->ij", qd, kd)
+    np.testing.assert_array_equal(o[0, 0, 0], vd[0])
+    for i in range(1, 15):
+        w = 1.0 / (1.0 + math.exp(s[i, i - 1] - s[i, i]))
+        np.testing.assert_allclose(o[0, i, 0], w * vd[i] + (1 - w) * vd[i - 1], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[0, 0, i], np.logaddexp(s[i, i], s[i, i - 1]), rtol=0, atol=1e-13)
+
+
+def test_window_reductions():
+    """A right side of 0 is bottom-right causal; sides at least the sequence
+    long are no window; window and causal masks intersect."""
+    q, k, v = _rand(1, 2, 1, 13, 29, 16, seed=34)
+    a = oracle.attn_fwd(q, k, v, 2, 0.3)
+    b = oracle.attn_fwd(q, k, v, 0, 0.3, window=(-1, 0))
+    c = oracle.attn_fwd(q, k, v, 0, 0.3, window=(28 + 13, 0))
+    assert all(np.array_equal(x, y) for x, y in zip(a, b)) and all(np.array_equal(x, y) for x, y in zip(a, c))
+    e = oracle.attn_fwd(q, k, v, 0, 0.3)
+    f = oracle.attn_fwd(q, k, v, 0, 0.3, window=(100, 100))
+    assert all(np.array_equal(x, y) for x, y in zip(e, f))
+    g = oracle.attn_fwd(q, k, v, 2, 0.3, window=(5, 9))
+    h = oracle.attn_fwd(q, k, v, 0, 0.3, window=(5, 0))
+    assert all(np.array_equal(x, y) for x, y in zip(g, h))
+
+
+def test_window_query_block_at_the_end_is_the_full_pass():
+    """Bottom-right alignment puts a query block of Nq rows at the last Nq
+    positions of the cache: its rows equal those rows of one windowed pass
+    with Nq = Nk = L (both with and without per-sequence lengths)."""
+    B, Hq, Hkv, Nq, S, d = 2, 4, 2, 6, 33, 16
+    q, k, v = _rand(B, Hq, Hkv, S, S, d, seed=35)
+    for wl, wr in [(4, 0), (7, 2), (3, -1)]:
+        for b, L in enumerate([33, 14]):
+            o_full, l_full = oracle.attn_fwd(q[b:b + 1, :L], k[b:b + 1, :L], v[b:b + 1, :L], 0, 0.2, window=(wl, wr))
+            qs = q[b:b + 1, L - Nq:L].contiguous()
+            o_t, l_t = oracle.attn_fwd(qs, k[b:b + 1], v[b:b + 1], 0, 0.2, kv_len=[L], window=(wl, wr))
+            np.testing.assert_allclose(o_t, o_full[:, L - Nq:L], rtol=0, atol=1e-13)
+            np.testing.assert_allclose(l_t, l_full[:, :, L - Nq:L], rtol=0, atol=1e-13)
+
+
+def test_window_never_reads_keys_outside_it():
+    """Keys and values outside every row's band may hold NaN: nothing changes."""
+    Nq = Nk = 24
+    q, k, v = _rand(1, 2, 2, Nq, Nk, 16, seed=36)
+    wl, wr = 3, 1
+    a = oracle.attn_fwd(q, k, v, 0, 0.3, window=(wl, wr))
+    # rows 10..13 only: keys 7..14 are in some band, the rest are poisoned
+    rows = np.array([(0, h, i) for h in range(2) for i in range(10, 14)], dtype=np.int32)
+    k2, v2 = k.clone(), v.clone()
+    for x in (k2, v2):
+        x[:, :7] = float("nan")
+        x[:, 15:] = float("nan")
+    o_r, l_r = oracle.attn_rows(q, k2, v2, rows, 0, 0.3, window=(wl, wr))
+    exp_o = np.stack([a[0][0, i, h] for _, h, i in rows])
+    exp_l = np.array([a[1][0, h, i] for _, h, i in rows])
+    assert np.array_equal(o_r, exp_o) and np.array_equal(l_r, exp_l)
