@@ -4,7 +4,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 One step = one call of the hot path over one batch of synthetic input:
-attn_fwd for the prefill / training workloads (one kernel launch), or
+attn_fwd for the prefill / training workloads (one kernel launch),
+attn_fwd_window for the sliding-window workload (one kernel launch), or
 attn_fwd_splitkv for the decode workload (split kernel + combine kernel).
 Default workload: the training shape B=4, H=16, N=4096, d=128, causal.
 
@@ -149,7 +150,7 @@ class ClockSampler:
 def get_workload(name):
     from exact_io_aware_14_gb300 import workloads as W
     table = {"tiny": W.TINY, "train_causal": W.TRAIN_CAUSAL, "train": W.TRAIN, "gqa": W.GQA, "long": W.LONG,
-             "decode": W.DECODE, "decode_paged": W.DECODE_PAGED}
+             "window": W.WINDOW, "decode": W.DECODE, "decode_paged": W.DECODE_PAGED}
     return table[name]
 
 
@@ -164,6 +165,9 @@ def config_of(w, n_gpus):
     else:
         cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.N, "Nk": w.N, "d": w.d,
                "causal": w.causal, "scale": "1/sqrt(d)"}
+        if w.window is not None:
+            cfg["window"] = list(w.window)
+            cfg["flops"] = "4*d per visible (row, key) pair"
     cfg["l2"] = "flushed before every timed step (256 MB write)"
     cfg["parallelism"] = "replicas x%d (independent, no exchange)" % n_gpus if n_gpus > 1 else "single GPU"
     return cfg
@@ -184,20 +188,22 @@ def oracle_sample_rate(w, q, k, v, seqlens, budget_s, seed):
     threads = oracle.host_threads()
     dec = isinstance(w, W.Decode)
     Nq = 1 if dec else w.N
+    keys = None if dec else w.keys_per_row().tolist()
 
     def rows_and_work(n):
         rows = W.sample_rows(w.B, w.Hq, Nq, n, seed=seed)
         if dec:
             work = sum(2 * int(seqlens[b]) * w.d * 2 for b, _, _ in rows)   # bytes of K and V rows read
         else:
-            work = sum(4.0 * ((i + 1) if w.causal else w.N) * w.d for _, _, i in rows)  # FLOPs
+            work = sum(4.0 * keys[i] * w.d for _, _, i in rows)  # FLOPs
         return rows, work
 
     def run(n):
         rows, work = rows_and_work(n)
         t0 = time.perf_counter()
         oracle.attn_rows(q, k, v, rows, False if dec else w.causal, w.scale,
-                         kv_len=(seqlens if dec else None), n_threads=threads)
+                         kv_len=(seqlens if dec else None), n_threads=threads,
+                         window=(None if dec else w.window))
         return work, time.perf_counter() - t0, len(rows)
 
     n = max(threads, 16)
@@ -314,10 +320,16 @@ def run_ours(args, w, rank, world, local_rank):
         unit, scale_unit = "TFLOP/s", 1e12
         launches_per_step = 1
 
-        def step():
-            rc = _native.attn_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
-            if rc != 0:
-                raise RuntimeError("attn_fwd: %s" % _native.status_string(rc))
+        if w.window is None:
+            def step():
+                rc = _native.attn_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+                if rc != 0:
+                    raise RuntimeError("attn_fwd: %s" % _native.status_string(rc))
+        else:
+            def step():
+                rc = _native.attn_fwd_window(q, k, v, o, lse, w.causal, w.window, w.scale, stream)
+                if rc != 0:
+                    raise RuntimeError("attn_fwd_window: %s" % _native.status_string(rc))
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -461,7 +473,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="train_causal",
-                    choices=["tiny", "train_causal", "train", "gqa", "long", "decode", "decode_paged"])
+                    choices=["tiny", "train_causal", "train", "gqa", "long", "window", "decode", "decode_paged"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--reference-seconds", type=float, default=90.0, help="whole reference-arm budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -46,8 +46,10 @@ def lib():
         vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         L.attn_fwd.restype = i
         L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+        L.attn_fwd_window.restype = i
+        L.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
         L.attn_fwd_kvcache.restype = i
-        L.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, f, vp]
+        L.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, i, i, f, vp]
         L.attn_splitkv_workspace_size.restype = sz
         L.attn_splitkv_workspace_size.argtypes = [i, i, i, i, i]
         L.attn_fwd_splitkv.restype = i
@@ -85,8 +87,7 @@ def _check_bf16(name, t, shape):
 
 
 # --------------------------------------------------------------------------- raw entry points
-def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
-    """Same contract as the C call: writes o [B,Nq,Hq,d] and lse [B,Hq,Nq]. Returns the status."""
+def _check_prefill(q, k, v, o, lse):
     B, Nq, Hq, d = q.shape
     Nk, Hkv = k.shape[1], k.shape[2]
     _check_bf16("q", q, (B, Nq, Hq, d))
@@ -95,11 +96,33 @@ def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
     _check_bf16("o", o, (B, Nq, Hq, d))
     if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("lse must be a contiguous CUDA fp32 tensor of shape %s" % ((B, Hq, Nq),))
+    return B, Hq, Hkv, Nq, Nk, d
+
+
+def _window(window):
+    """None or (left, right); a negative side is unbounded."""
+    if window is None:
+        return -1, -1
+    wl, wr = (int(x) for x in window)
+    return wl, wr
+
+
+def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
+    """Same contract as the C call: writes o [B,Nq,Hq,d] and lse [B,Hq,Nq]. Returns the status."""
+    B, Hq, Hkv, Nq, Nk, d = _check_prefill(q, k, v, o, lse)
     return lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                           int(causal), float(scale), _stream_handle(stream))
 
 
-def attn_fwd_kvcache(q, k_cache, v_cache, seqlens, o, lse, causal, scale, stream=None):
+def attn_fwd_window(q, k, v, o, lse, causal, window, scale, stream=None):
+    """attn_fwd with a local window (left, right), aligned bottom-right. Returns the status."""
+    B, Hq, Hkv, Nq, Nk, d = _check_prefill(q, k, v, o, lse)
+    wl, wr = _window(window)
+    return lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                 int(causal), wl, wr, float(scale), _stream_handle(stream))
+
+
+def attn_fwd_kvcache(q, k_cache, v_cache, seqlens, o, lse, causal, scale, stream=None, window=None):
     """Same contract as the C call: q, o [B,Nq,Hq,d]; caches [B,max_seqlen,Hkv,d];
     seqlens int32 [B] on the device; lse [B,Hq,Nq].  Returns the status."""
     B, Nq, Hq, d = q.shape
@@ -112,16 +135,18 @@ def attn_fwd_kvcache(q, k_cache, v_cache, seqlens, o, lse, causal, scale, stream
         raise ValueError("seqlens must be a CUDA int32 tensor of shape (%d,)" % B)
     if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("lse must be a contiguous CUDA fp32 tensor of shape %s" % ((B, Hq, Nq),))
+    wl, wr = _window(window)
     return lib().attn_fwd_kvcache(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), max_seqlen, _ptr(o),
-                                  _ptr(lse), B, Hq, Hkv, Nq, d, int(causal), float(scale), _stream_handle(stream))
+                                  _ptr(lse), B, Hq, Hkv, Nq, d, int(causal), wl, wr, float(scale),
+                                  _stream_handle(stream))
 
 
-def forward_kvcache(q, k_cache, v_cache, seqlens, causal, scale, stream=None):
+def forward_kvcache(q, k_cache, v_cache, seqlens, causal, scale, stream=None, window=None):
     """Allocates O and LSE and runs attn_fwd_kvcache. Returns (o, lse)."""
     B, Nq, Hq, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
-    rc = attn_fwd_kvcache(q, k_cache, v_cache, seqlens, o, lse, causal, scale, stream)
+    rc = attn_fwd_kvcache(q, k_cache, v_cache, seqlens, o, lse, causal, scale, stream, window)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_kvcache")
     return o, lse
@@ -204,6 +229,17 @@ def forward(q, k, v, causal, scale, stream=None):
     rc = attn_fwd(q, k, v, o, lse, causal, scale, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return o, lse
+
+
+def forward_window(q, k, v, causal, window, scale, stream=None):
+    """Allocates O and LSE and runs attn_fwd_window. Returns (o, lse)."""
+    B, Nq, Hq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    rc = attn_fwd_window(q, k, v, o, lse, causal, window, scale, stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_window")
     return o, lse
 
 

@@ -70,21 +70,36 @@ const char* attn_status_string(attn_status s) {
   return "unknown status";
 }
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                     int Nq, int Nk, int d, int causal, float scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// A window side of Nq + Nk or more bounds nothing: it is made unbounded (-1),
+// which also keeps every position sum inside int range.
+int normalise_window(int w, int Nq, int Nk) {
+  if (w < 0) return -1;
+  return static_cast<long long>(w) >= static_cast<long long>(Nq) + Nk ? -1 : w;
+}
+
+// Shared by attn_fwd, attn_fwd_window and attn_fwd_kvcache.  Nk is the
+// allocated key length (max_seqlen for a cache); seqlens is null or a device
+// array of per-sequence key counts.
+attn_status prefill(const void* q, const void* k, const void* v, const int* seqlens, void* o, float* lse, int B,
+                    int Hq, int Hkv, int Nq, int Nk, int d, int causal, int window_left, int window_right,
+                    float scale, void* stream) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0 || (Hq % Hkv) != 0) return ATTN_ERR_INVALID_ARG;
   if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   // 32-bit TMA coordinates and grid: keep rows and tiles well inside int range
-  if (static_cast<long long>(Nq) + 127 > 0x7fffffffLL || static_cast<long long>(Nk) + 127 > 0x7fffffffLL)
-    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(Nq) + Nk + 256 > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>((Nq + 127) / 128) * B * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (Nq == 0) return ATTN_OK;
   if (!q || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (Nk > 0 && (!k || !v)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_MISALIGNED;
   if (Nk > 0 && (!aligned16(k) || !aligned16(v))) return ATTN_ERR_MISALIGNED;
+  if (seqlens && (reinterpret_cast<uintptr_t>(seqlens) & 3u)) return ATTN_ERR_MISALIGNED;
 
   attn::PrefillParams p;
   std::memset(&p, 0, sizeof p);
@@ -105,44 +120,35 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.Nk = Nk;
   p.d = d;
   p.causal = causal;
-  p.seqlens = nullptr;
+  p.seqlens = seqlens;
+  p.window_left = normalise_window(window_left, Nq, Nk);
+  p.window_right = normalise_window(window_right, Nq, Nk);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
   return attn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, int causal, float scale, void* stream) {
+  return prefill(q, k, v, nullptr, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, -1, -1, scale, stream);
+}
+
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                            int Hkv, int Nq, int Nk, int d, int causal, int window_left, int window_right, float scale,
+                            void* stream) {
+  return prefill(q, k, v, nullptr, o, lse, B, Hq, Hkv, Nq, Nk, d, causal, window_left, window_right, scale, stream);
+}
+
 attn_status attn_fwd_kvcache(const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
                              int max_seqlen, void* o, float* lse, int B, int Hq, int Hkv, int Nq, int d, int causal,
-                             float scale, void* stream) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 0 || max_seqlen < 1 || (Hq % Hkv) != 0) return ATTN_ERR_INVALID_ARG;
-  if (causal < 0 || causal > 2) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  if (static_cast<long long>(Nq) + 127 > 0x7fffffffLL || static_cast<long long>(max_seqlen) + 127 > 0x7fffffffLL)
-    return ATTN_ERR_UNSUPPORTED;
-  if (static_cast<long long>((Nq + 127) / 128) * B * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  if (Nq == 0) return ATTN_OK;
-  if (!q || !k_cache || !v_cache || !seqlens || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(o) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
-    return ATTN_ERR_MISALIGNED;
-
-  attn::PrefillParams p;
-  std::memset(&p, 0, sizeof p);
-  if (!make_map(&p.tm_q, q, B, Nq, Hq, d, 128) || !make_map(&p.tm_k, k_cache, B, max_seqlen, Hkv, d, 128) ||
-      !make_map(&p.tm_v, v_cache, B, max_seqlen, Hkv, d, 128))
-    return ATTN_ERR_LAUNCH;
-  p.o = o;
-  p.lse = lse;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.Nq = Nq;
-  p.Nk = max_seqlen;
-  p.d = d;
-  p.causal = causal;
-  p.seqlens = seqlens;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
-  return attn::launch_prefill(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+                             int window_left, int window_right, float scale, void* stream) {
+  if (max_seqlen < 1) return ATTN_ERR_INVALID_ARG;
+  if (Nq > 0 && (!k_cache || !v_cache || !seqlens)) return ATTN_ERR_INVALID_ARG;
+  return prefill(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Nq, max_seqlen, d, causal, window_left,
+                 window_right, scale, stream);
 }
 
 size_t attn_splitkv_workspace_size(int B, int Hq, int max_seqlen, int d, int chunk) {

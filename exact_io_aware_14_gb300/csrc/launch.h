@@ -19,6 +19,7 @@ struct PrefillParams {
   int B, Hq, Hkv, Nq, Nk, d;
   int causal;            // 0 none, 1 aligned top-left, 2 aligned bottom-right
   const int* seqlens;    // null, or keys per sequence (cache lengths <= Nk) on the device
+  int window_left, window_right;  // local window aligned bottom-right; -1: that side unbounded
   float scale_log2;      // scale * log2(e)
 };
 cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);

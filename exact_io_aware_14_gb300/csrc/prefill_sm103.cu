@@ -103,8 +103,9 @@ constexpr float kRescaleLog2 = 8.f;
 
 // Row max of one 128-column score tile in TMEM (this thread's lane), read in
 // two 64-column halves.  kNeg: the scale is negative, work on -s.
-template <bool kMasked, bool kNeg>
-__device__ __forceinline__ float score_tile_max(uint32_t tS, int lim) {
+// Masked tiles keep columns [lo, lim) (kLo) or [0, lim).
+template <bool kMasked, bool kNeg, bool kLo = false>
+__device__ __forceinline__ float score_tile_max(uint32_t tS, int lo, int lim) {
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -119,7 +120,7 @@ __device__ __forceinline__ float score_tile_max(uint32_t tS, int lim) {
       for (int k = 0; k < 4; ++k) {
         v[k] = __uint_as_float(u[(i + k) >> 5][(i + k) & 31]);
         if (kNeg) v[k] = -v[k];
-        if (kMasked) v[k] = (64 * h + i + k < lim) ? v[k] : -INFINITY;
+        if (kMasked) v[k] = (64 * h + i + k < lim && (!kLo || 64 * h + i + k >= lo)) ? v[k] : -INFINITY;
       }
       mx0 = fmax3(mx0, v[0], v[1]);
       mx1 = fmax3(mx1, v[2], v[3]);
@@ -131,8 +132,8 @@ __device__ __forceinline__ float score_tile_max(uint32_t tS, int lim) {
 // p = 2^(s*c - mc) for the 128 scores of this lane, written back as bf16
 // pairs over the first 64 columns (half h of P only overwrites scores already
 // consumed).  Returns the row sum of the fp32 p.
-template <bool kMasked, bool kNeg>
-__device__ __forceinline__ float score_tile_exp(uint32_t tS, int lim, float c, float mc) {
+template <bool kMasked, bool kNeg, bool kLo = false>
+__device__ __forceinline__ float score_tile_exp(uint32_t tS, int lo, int lim, float c, float mc) {
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
   const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
 #pragma unroll 1
@@ -154,8 +155,8 @@ __device__ __forceinline__ float score_tile_exp(uint32_t tS, int lim, float c, f
       float p0 = ex2_approx(x.x);
       float p1 = ex2_approx(x.y);
       if (kMasked) {  // also right for c == 0, where -inf * 0 would not give 0
-        p0 = (64 * h + 2 * i < lim) ? p0 : 0.f;
-        p1 = (64 * h + 2 * i + 1 < lim) ? p1 : 0.f;
+        p0 = (64 * h + 2 * i < lim && (!kLo || 64 * h + 2 * i >= lo)) ? p0 : 0.f;
+        p1 = (64 * h + 2 * i + 1 < lim && (!kLo || 64 * h + 2 * i + 1 >= lo)) ? p1 : 0.f;
       }
       if (i & 1)
         acc1 = fadd2(acc1, make_float2(p0, p1));
@@ -169,23 +170,30 @@ __device__ __forceinline__ float score_tile_exp(uint32_t tS, int lim, float c, f
 }
 
 // Work unit U -> (batch, KV head, the two query tiles).  Units are numbered
-// (u_rev, head slot, batch) with u_rev slowest, so causal units come longest
+// (u_rev, head slot, batch) with u_rev slowest, so units whose rows see a
+// right-bounded key range (causal, or a window's right side) come longest
 // first.  Keys of the unit's sequence: nk (Nk, or its cache length when
-// seqlens is given); causal mode 1 aligns top-left, 2 bottom-right (key j
-// visible to row i iff j <= i + coff).
+// seqlens is given); key j is visible to row i iff j < nk, j <= i + coff and,
+// in the general form, j >= i + lo.  causal 1 aligns top-left (coff = 0), 2
+// bottom-right (coff = nk - Nq); a local window (wl, wr) is aligned
+// bottom-right: row i sits at key position i + nk - Nq and sees wl keys
+// before it and wr after it (negative: that side unbounded).  The unit's key
+// tiles are kt0 .. kt0 + n_kt - 1; tile t visits the first ti[t].n_kt of them.
 struct Unit {
   int b, hkv, n_kt;
-  int nk, coff;
+  int nk, coff, lo, kt0;
   TileInfo ti[2];
 };
-__device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
+template <bool kGeneral>
+__device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal, int wl, int wr,
                                             const int* __restrict__ seqlens, int pair_heads, int units_per_bh) {
   Unit u;
   const int hslots = pair_heads ? Hq / 2 : Hq;
   const int bh_count = B * hslots;
   const int u_rev = U / bh_count;
   const int bh = U % bh_count;
-  const int unit = causal ? (units_per_bh - 1 - u_rev) : u_rev;
+  const bool rev = (causal != 0) || (kGeneral && wr >= 0);
+  const int unit = rev ? (units_per_bh - 1 - u_rev) : u_rev;
   u.b = bh / hslots;
   const int hs = bh % hslots;
   if (pair_heads) {
@@ -199,11 +207,36 @@ __device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int N
   }
   u.hkv = u.ti[0].hq / (Hq / Hkv);  // both heads of a pair share the KV head
   u.nk = seqlens ? min(max(seqlens[u.b], 0), Nk) : Nk;
-  u.coff = (causal == 2) ? u.nk - Nq : 0;
+  if (!kGeneral) {
+    u.coff = (causal == 2) ? u.nk - Nq : 0;
+    u.lo = 0;
+    u.kt0 = 0;
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int kend = causal ? max(0, min(u.nk, u.ti[t].row0 + BM + u.coff)) : u.nk;
-    u.ti[t].n_kt = (u.ti[t].row0 < Nq) ? (kend + BN - 1) / BN : 0;
+    for (int t = 0; t < 2; ++t) {
+      const int kend = causal ? max(0, min(u.nk, u.ti[t].row0 + BM + u.coff)) : u.nk;
+      u.ti[t].n_kt = (u.ti[t].row0 < Nq) ? (kend + BN - 1) / BN : 0;
+    }
+  } else {
+    const int pos0 = u.nk - Nq;  // key position of query row 0
+    int hi = u.nk;               // no right bound
+    if (causal) hi = (causal == 2) ? pos0 : 0;
+    if (wr >= 0) hi = min(hi, pos0 + wr);
+    u.coff = hi;
+    u.lo = (wl >= 0) ? pos0 - wl : -(Nq + BM);  // -(Nq + BM): no left bound for any row of a tile
+    int kend[2], first = u.nk;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      // keys some row of the tile sees: [row0 + lo, row0 + BM - 1 + hi] within [0, nk)
+      const int kbeg = max(0, u.ti[t].row0 + u.lo);
+      kend[t] = min(u.nk, u.ti[t].row0 + BM + hi);
+      if (u.ti[t].row0 >= Nq || kend[t] <= kbeg)
+        kend[t] = 0;
+      else
+        first = min(first, kbeg);
+    }
+    u.kt0 = first / BN;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) u.ti[t].n_kt = kend[t] > 0 ? (kend[t] + BN - 1) / BN - u.kt0 : 0;
   }
   u.n_kt = max(u.ti[0].n_kt, u.ti[1].n_kt);
   return u;
@@ -221,18 +254,19 @@ __device__ __forceinline__ int unit_of_round(int r, int total_units) {
 // Barrier phases run on across units: per-unit barriers by the unit count
 // `uc`, score / P barriers by the running key-tile count of each query tile,
 // ring slots by the running item count.
-// kCache: keys per sequence come from seqlens (attn_fwd_kvcache); otherwise
-// every sequence has Nk keys and seqlens is not read.
-template <int D, bool kNeg, bool kCache>
+// kGeneral: keys per sequence may come from seqlens (attn_fwd_kvcache) and
+// the mask may have a local window; otherwise every sequence has Nk keys,
+// seqlens is not read and the mask is at most causal.
+template <int D, bool kNeg, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                        float* __restrict__ lse_out, int B, int Hq, int Hkv, int Nq, int Nk, int causal,
-                       const int* __restrict__ seqlens,
+                       int wl, int wr, const int* __restrict__ seqlens,
                        float scale_log2, int pair_heads, int units_per_bh, int total_units) {
   using L = Layout<D>;
   constexpr int NS = L::kSlots;
-  const int* const lens = kCache ? seqlens : nullptr;
+  const int* const lens = kGeneral ? seqlens : nullptr;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -293,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, lens, pair_heads, units_per_bh);
-        if (kCache && (lens[u.b] < 0 || lens[u.b] > Nk) && u.ti[0].hq == 0) record(11, kDevBadSeqlen);
+        const Unit u = decode_unit<kGeneral>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads, units_per_bh);
+        if (kGeneral && lens && (lens[u.b] < 0 || lens[u.b] > Nk) && u.ti[0].hq == 0) record(11, kDevBadSeqlen);
         for (int t = 0; t < 2; ++t) {
           // Q_t of the previous unit must have been read by its last QK^T
           if (uc >= 1 && !wait_one(bar_qfree + t, (uc - 1) & 1, abort_flag, 1)) { ok = false; break; }
@@ -314,13 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // hold anything, NaN included (and P = 0 times NaN is not 0): it is
           // loaded against a private barrier and those rows are cleared before
           // the MMA thread is told the tile is there.
-          const int valid = u.nk - kt * BN;
-          const bool fix = kCache && is_v && valid < BN;
+          const int valid = u.nk - (u.kt0 + kt) * BN;
+          const bool fix = kGeneral && lens && is_v && valid < BN;
           uint64_t* done = fix ? bar_vfix : bar_full + slot;
           mbar_arrive_expect_tx(done, L::kTile);
           for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, done, h * 64, u.hkv, kt * BN,
-                        u.b);
+            tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, done, h * 64, u.hkv,
+                        (u.kt0 + kt) * BN, u.b);
           if (fix) {
             if (!wait_one(bar_vfix, vfix_uses & 1, abort_flag, 12)) { ok = false; break; }
             ++vfix_uses;
@@ -354,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, lens, pair_heads, units_per_bh);
+        const Unit u = decode_unit<kGeneral>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads, units_per_bh);
         const int n_kt = u.n_kt;
         for (int t = 0; t < 2 && ok; ++t) {
           ok = wait_one(bar_qfull + t, uc & 1, abort_flag, 3);
@@ -509,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
       const int U = unit_of_round(rnd, total_units);
       if (U < 0) continue;
-      const Unit u = decode_unit(U, B, Hq, Hkv, Nq, Nk, causal, lens, pair_heads, units_per_bh);
+      const Unit u = decode_unit<kGeneral>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads, units_per_bh);
       const TileInfo me = t ? u.ti[1] : u.ti[0];
       const int grow = me.row0 + r;
       const int my_kt = me.n_kt;
@@ -518,22 +552,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < my_kt; ++j) {
         if (!wait_all(bar_sfull + t, (kc + j) & 1, abort_flag, 7)) { ok = false; break; }
         tc_fence_after();
-        const int kbase = j * BN;
-        const bool masked = (kbase + BN > u.nk) || (causal && kbase + BN - 1 > me.row0 + u.coff);
-        int lim = BN;  // columns [lim, BN) of this tile are masked for this row
-        if (masked) {
-          lim = u.nk - kbase;
-          if (causal) lim = min(lim, grow + u.coff - kbase + 1);
+        const int kbase = (u.kt0 + j) * BN;
+        bool masked;
+        int lim = BN, lo = 0;  // columns outside [lo, lim) of this tile are masked for this row
+        if (kGeneral) {
+          masked = (kbase + BN > u.nk) || (kbase + BN - 1 > me.row0 + u.coff) || (kbase < me.row0 + BM - 1 + u.lo);
+          if (masked) {
+            lim = min(u.nk - kbase, grow + u.coff - kbase + 1);
+            lo = grow + u.lo - kbase;
+          }
+        } else {
+          masked = (kbase + BN > u.nk) || (causal && kbase + BN - 1 > me.row0 + u.coff);
+          if (masked) {
+            lim = u.nk - kbase;
+            if (causal) lim = min(lim, grow + u.coff - kbase + 1);
+          }
         }
-        const float mt = masked ? score_tile_max<true, kNeg>(tS, lim) : score_tile_max<false, kNeg>(tS, lim);
+        const float mt = masked ? score_tile_max<true, kNeg, kGeneral>(tS, lo, lim)
+                                : score_tile_max<false, kNeg>(tS, lo, lim);
         // move the reference only on the first visible scores or when the tile
         // max is more than 2^kRescaleLog2 above it
         const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
         const float m_new = need ? fmaxf(m, mt) : m;
         const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
         const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
-        const float rowsum = masked ? score_tile_exp<true, kNeg>(tS, lim, c, mc)
-                                    : score_tile_exp<false, kNeg>(tS, lim, c, mc);
+        const float rowsum = masked ? score_tile_exp<true, kNeg, kGeneral>(tS, lo, lim, c, mc)
+                                    : score_tile_exp<false, kNeg>(tS, lo, lim, c, mc);
         l = l * alpha + rowsum;
 
         // O_t holds the sum through tile j-1 (P.V of j-1 completed before S_j was
@@ -634,12 +678,14 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(total < n_sm ? total : n_sm);  // one persistent CTA per SM
-  auto kern = p.seqlens ? ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, true> : prefill_fwd_kernel<D, false, true>)
-                        : ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, false> : prefill_fwd_kernel<D, false, false>);
+  const bool general = p.seqlens || p.window_left >= 0 || p.window_right >= 0;
+  auto kern = general ? ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, true> : prefill_fwd_kernel<D, false, true>)
+                      : ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, false> : prefill_fwd_kernel<D, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, L::kAlloc, stream>>>(p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B,
-                                              p.Hq, p.Hkv, p.Nq, p.Nk, p.causal, p.seqlens, p.scale_log2, pair_heads,
+                                              p.Hq, p.Hkv, p.Nq, p.Nk, p.causal, p.window_left, p.window_right,
+                                              p.seqlens, p.scale_log2, pair_heads,
                                               units_per_bh, static_cast<int>(total));
   return cudaGetLastError();
 }

@@ -28,13 +28,32 @@ class Prefill:
     causal: bool
     amp: float = 1.0
     seed: int = 0
+    window: tuple = None  # local window (left, right), aligned bottom-right; None: no window
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
+    def keys_per_row(self):
+        """How many keys each query row sees (int64 [N]); for work accounting."""
+        i = torch.arange(self.N, dtype=torch.int64)
+        lo = torch.zeros_like(i)
+        hi = torch.full_like(i, self.N - 1)
+        if self.causal:
+            hi = torch.minimum(hi, i)
+        if self.window is not None:
+            wl, wr = self.window
+            if wl >= 0:
+                lo = torch.maximum(lo, i - wl)
+            if wr >= 0:
+                hi = torch.minimum(hi, i + wr)
+        return (hi - lo + 1).clamp(min=0)
+
     def flops(self) -> float:
-        """4*B*Hq*Nq*Nk*d, halved for causal (the workload's FLOP convention)."""
+        """4*B*Hq*Nq*Nk*d, halved for causal (the workload's FLOP convention);
+        with a window, 4*B*Hq*d times the pairs the window leaves visible."""
+        if self.window is not None:
+            return 4.0 * self.B * self.Hq * self.d * float(self.keys_per_row().sum())
         f = 4.0 * self.B * self.Hq * self.N * self.N * self.d
         return f / 2 if self.causal else f
 
@@ -59,18 +78,22 @@ class Decode:
 
 
 # The workloads: tiny parity case, training shape (causal and not), GQA
-# prefill, long single sequence, split-KV decode.
+# prefill, long single sequence, sliding window, split-KV decode.
 TINY = Prefill("tiny_mha_b1_h2_n256_d64", 1, 2, 2, 256, 64, False, seed=0)
 TRAIN_CAUSAL = Prefill("train_b4_h16_n4096_d128_causal", 4, 16, 16, 4096, 128, True, seed=1)
 TRAIN = Prefill("train_b4_h16_n4096_d128", 4, 16, 16, 4096, 128, False, seed=1)
 GQA = Prefill("gqa_prefill_b2_hq32_hkv8_n8192_d128_causal", 2, 32, 8, 8192, 128, True, amp=0.5, seed=2)
 LONG = Prefill("long_b1_h8_n32768_d128_causal", 1, 8, 8, 32768, 128, True, seed=3)
+# the pyshine.com tour's usage example (Hq 32, Hkv 8, N 2048, d 128, causal,
+# window (1023, 0)) with a batch of 16
+WINDOW = Prefill("window_b16_hq32_hkv8_n2048_d128_causal_w1023", 16, 32, 8, 2048, 128, True, seed=5,
+                 window=(1023, 0))
 DECODE = Decode("decode_b16_hq32_hkv8_len1024to16384_d128_chunk1024", 16, 32, 8, 16384, 128, 1024,
                 1024, 16384, seed=4)
 DECODE_PAGED = Decode("decode_paged_b16_hq32_hkv8_len1024to16384_d128_chunk1024_page256", 16, 32, 8, 16384, 128,
                       1024, 1024, 16384, seed=4, page_size=256)
 
-PREFILL_WORKLOADS = (TINY, TRAIN_CAUSAL, TRAIN, GQA, LONG)
+PREFILL_WORKLOADS = (TINY, TRAIN_CAUSAL, TRAIN, GQA, LONG, WINDOW)
 
 
 def _randn_bf16(gen, shape, amp):

@@ -15,7 +15,8 @@
  * Grouped heads: Hkv divides Hq and query head hq reads KV head
  * hq / (Hq / Hkv) (pyshine.com flash-attention tour, "Why You Need This":
  * K and V may carry fewer heads than Q when the counts divide).
- * Causal masking is aligned top-left: key j is visible to row i iff j <= i.
+ * Masks: causal aligned top-left (key j visible to row i iff j <= i) or
+ * bottom-right, and a local window (attn_fwd_window, attn_fwd_kvcache).
  * A row that sees no key gets O = 0 and LSE = -inf.
  *
  * Layout: every tensor is dense and row-major, BSHD with d innermost:
@@ -86,11 +87,31 @@ typedef enum {
  * FA4 paragraphs); key tiles wholly above the causal diagonal are skipped.
  * Constraints: B, Hq, Hkv >= 1; Nq >= 0; Nk >= 0; Hq % Hkv == 0;
  * d in {64, 128}; all pointers 16-byte aligned (lse: 4-byte) and non-NULL
- * unless B*Nq == 0.  Sizes must keep every tensor below 2^31 rows.
+ * unless B*Nq == 0.  Nq + Nk must stay below 2^31 - 256.
  */
 ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int Hq, int Hkv, int Nq, int Nk, int d,
                      int causal, float scale, void* stream);
+
+/*
+ * Local (sliding-window) attention: attn_fwd with a window (window_left,
+ * window_right).  Query row i sits at key position pos_i = i + Nk - Nq
+ * (aligned bottom-right) and sees key j only if
+ *     pos_i - window_left <= j <= pos_i + window_right
+ * ("FlashAttention: Part 2", section 3.2: local attention keeps i -> j only
+ * for |i - j| <= w; the pyshine.com tour, "From Install to Causal
+ * Attention", passes the window as a (left, right) pair next to causal, as
+ * in causal with (1023, 0)).  A negative side is unbounded; (-1, -1) is
+ * attn_fwd.  The window intersects the causal mask chosen by `causal`;
+ * with causal = 0, (w, 0) is bottom-right causal attention over the last
+ * w + 1 keys.  Key tiles outside every row's window are never loaded.
+ * Arguments, constraints and errors otherwise as for attn_fwd; the inputs
+ * must be finite wherever a tile is loaded (keys of [0, Nk) in tiles that
+ * some row's window touches).
+ */
+ATTN_API attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                     int window_left, int window_right, float scale, void* stream);
 
 /*
  * The same forward against a KV cache with a length per sequence: a block
@@ -105,13 +126,16 @@ ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void*
  *   causal: as for attn_fwd, with Nk = seqlens[b]: ATTN_CAUSAL_BOTTOM_RIGHT
  *            puts query row i at cache position seqlens[b] - Nq + i (the
  *            new rows are the last Nq keys of the cache).
+ *   window_left, window_right: a local window as for attn_fwd_window,
+ *            positions taken with Nk = seqlens[b]; -1, -1 for none.
  * Constraints and errors are those of attn_fwd; a seqlens entry outside
  * [0, max_seqlen] is clamped and reported as ATTN_ERR_DEVICE_ARG by
  * attn_get_device_status.
  */
 ATTN_API attn_status attn_fwd_kvcache(const void* q, const void* k_cache, const void* v_cache,
                              const int* seqlens, int max_seqlen, void* o, float* lse,
-                             int B, int Hq, int Hkv, int Nq, int d, int causal, float scale, void* stream);
+                             int B, int Hq, int Hkv, int Nq, int d, int causal,
+                             int window_left, int window_right, float scale, void* stream);
 
 /*
  * Bytes of workspace attn_fwd_splitkv needs: fp32 partial outputs and

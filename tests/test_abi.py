@@ -113,11 +113,13 @@ def test_paged_splitkv_argument_checks(L):
 
 
 def _kvc(L, **kw):
-    a = dict(q=16, k=16, v=16, s=16, S=512, o=16, lse=16, B=2, Hq=8, Hkv=2, Nq=40, d=128, causal=2, scale=0.1)
+    a = dict(q=16, k=16, v=16, s=16, S=512, o=16, lse=16, B=2, Hq=8, Hkv=2, Nq=40, d=128, causal=2, wl=-1, wr=-1,
+             scale=0.1)
     a.update(kw)
     vp = lambda x: ctypes.c_void_p(x) if x else None
     return L.attn_fwd_kvcache(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["s"]), a["S"], vp(a["o"]), vp(a["lse"]),
-                              a["B"], a["Hq"], a["Hkv"], a["Nq"], a["d"], a["causal"], a["scale"], None)
+                              a["B"], a["Hq"], a["Hkv"], a["Nq"], a["d"], a["causal"], a["wl"], a["wr"],
+                              a["scale"], None)
 
 
 def test_kvcache_argument_checks(L):
@@ -129,3 +131,28 @@ def test_kvcache_argument_checks(L):
     assert _kvc(L, k=24) == 3
     assert _kvc(L, s=18) == 3                 # misaligned lengths
     assert _kvc(L, Nq=0) == 0                 # nothing to do
+
+
+def _win(L, **kw):
+    a = dict(q=16, k=16, v=16, o=16, lse=16, B=2, Hq=8, Hkv=2, Nq=300, Nk=300, d=128, causal=0, wl=127, wr=0,
+             scale=0.1)
+    a.update(kw)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.attn_fwd_window(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["o"]), vp(a["lse"]), a["B"], a["Hq"],
+                             a["Hkv"], a["Nq"], a["Nk"], a["d"], a["causal"], a["wl"], a["wr"], a["scale"], None)
+
+
+def test_window_argument_checks(L):
+    """Host checks run before anything is launched (no GPU needed): every
+    window value is accepted (negative: unbounded side), the other checks
+    are those of attn_fwd."""
+    assert _win(L, causal=3) == 1
+    assert _win(L, Hq=6, Hkv=4) == 1
+    assert _win(L, d=96) == 2
+    assert _win(L, q=0) == 1
+    assert _win(L, k=8) == 3
+    assert _win(L, scale=float("nan")) == 1
+    assert _win(L, Nq=0) == 0
+    assert _win(L, Nq=0, wl=-7, wr=1 << 30) == 0
+    assert _win(L, Nq=(1 << 31) - 200, Nk=100) == 2   # Nq + Nk must leave room below 2^31
+    assert _kvc(L, Nq=0, wl=5, wr=-3) == 0
