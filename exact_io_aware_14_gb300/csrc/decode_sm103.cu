@@ -471,12 +471,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// One CTA per (b, hq), one thread per output dim.  It runs after the split
+// grid, on the critical path of the step, so its loads are issued together:
+// the split LSEs spread over the threads for a block-wide max, then the
+// weighted sum eight splits at a time (independent loads, one L2 round trip
+// per eight splits instead of one per split).
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ o_part,
                                                            const float* __restrict__ lse_part,
                                                            const int* __restrict__ seqlens, int max_seqlen, int Hq,
                                                            int chunk, int n_split, __nv_bfloat16* __restrict__ out,
                                                            float* __restrict__ lse_out) {
+  constexpr int kWarps = D / 32;
+  __shared__ float s_red[kWarps];
   const int b = blockIdx.x / Hq;
   const int hq = blockIdx.x % Hq;
   const int dd = threadIdx.x;
@@ -494,12 +501,35 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
   }
   const float* lp = lse_part + row * n_split;
   float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, lp[s]);
+  for (int s = dd; s < ns; s += D) mx = fmaxf(mx, lp[s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((dd & 31) == 0) s_red[dd >> 5] = mx;
+  __syncthreads();
+  mx = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) mx = fmaxf(mx, s_red[w]);
+  const float* op = o_part + row * n_split * D + dd;
   float tot = 0.f, acc = 0.f;
-  for (int s = 0; s < ns; ++s) {
+  int s = 0;
+  for (; s + 8 <= ns; s += 8) {
+    float l8[8], o8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      l8[i] = lp[s + i];
+      o8[i] = op[static_cast<size_t>(s + i) * D];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w = expf(l8[i] - mx);
+      tot += w;
+      acc = fmaf(w, o8[i], acc);
+    }
+  }
+  for (; s < ns; ++s) {
     const float w = expf(lp[s] - mx);
     tot += w;
-    acc = fmaf(w, o_part[(row * n_split + s) * D + dd], acc);
+    acc = fmaf(w, op[static_cast<size_t>(s) * D], acc);
   }
   out[row * D + dd] = __float2bfloat16_rn(acc / tot);
   if (dd == 0) lse_out[row] = mx + logf(tot);

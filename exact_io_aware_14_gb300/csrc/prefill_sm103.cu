@@ -404,21 +404,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // barrier is due, run in a branch-free loop (below); the others in the
         // general form.  Every instruction of this thread between two MMA
         // batches leaves the tensor core idle, so the loop keeps ring positions
-        // and barrier parities incrementally and probes the next step's K / V
-        // before its P wait.
+        // and barrier parities incrementally and probes the barriers it will
+        // wait on next (K_{j+1}, P_1, then the next step's V_j and P_0) right
+        // after issuing a batch, while the queued MMAs still run; a barrier
+        // found complete is not waited on again.
         const int n_both = min(u.ti[0].n_kt, u.ti[1].n_kt);
         const int j_steady_end = n_both - 2;
         for (int j = 0; ok && j <= n_kt;) {
           if (j >= 2 && j <= j_steady_end) {
-            // ring items: K_j = g, V_{j-1} = g+1, K_{j+1} = g+2.  V_{j-1} was
-            // loaded only after S_1(j-2) was complete, so it is awaited here,
-            // right before its first use, a step after the general form
-            // would; K_{j+1} is probed now and awaited after tile 0's MMAs.
+            // ring items: K_j = g, V_{j-1} = g+1, K_{j+1} = g+2, V_j = g+3.
+            // V_{j-1} was loaded only after S_1(j-2) was complete, so it is
+            // awaited right before its first use, a step after the general
+            // form would; K_{j+1} is awaited after tile 0's MMAs.
             const uint32_t g = item_base + 2 * j - 1;
             int s0 = static_cast<int>(g % NS);
             uint32_t ph0 = (g / NS) & 1u;
             uint32_t pp0 = static_cast<uint32_t>(kc[0] + j - 1) & 1u;
             uint32_t pp1 = static_cast<uint32_t>(kc[1] + j - 1) & 1u;
+            bool v_ready = false, p0_ready = false;  // probed during the previous step
             for (; j <= j_steady_end; ++j) {
               int s1 = s0 + 1;
               uint32_t ph1 = ph0;
@@ -426,23 +429,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               int s2 = s1 + 1;
               uint32_t ph2 = ph1;
               if (s2 >= NS) { s2 -= NS; ph2 ^= 1u; }
-              const bool k_ready = mbar_test_wait(bar_full + s2, ph2);
+              int s3 = s2 + 1;
+              uint32_t ph3 = ph2;
+              if (s3 >= NS) { s3 -= NS; ph3 ^= 1u; }
               const uint64_t dv = dV + static_cast<uint64_t>((s1 * L::kTile) >> 4);
               const uint64_t db = dK + static_cast<uint64_t>((s0 * L::kTile) >> 4);
-              if (!wait_one(bar_full + s1, ph1, abort_flag, 5)) { ok = false; break; }
-              if (!wait_one(bar_pfull + 0, pp0, abort_flag, 6)) { ok = false; break; }
+              if (!v_ready && !wait_one(bar_full + s1, ph1, abort_flag, 5)) { ok = false; break; }
+              if (!p0_ready && !wait_one(bar_pfull + 0, pp0, abort_flag, 6)) { ok = false; break; }
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk)
                 mma_bf16_ts(tmem + 256, tmem + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc_pv, 1u);
+              const bool k_ready = mbar_test_wait(bar_full + s2, ph2);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * L::kHalf + (kk & 3) * 32) >> 4;
                 mma_bf16_ss(tmem, dQ + off, db + off, idesc_qk, kk > 0 ? 1u : 0u);
               }
               mma_commit(bar_sfull + 0);
+              const bool p1_ready = mbar_test_wait(bar_pfull + 1, pp1);
               if (!k_ready && !wait_one(bar_full + s2, ph2, abort_flag, 4)) { ok = false; break; }
-              if (!wait_one(bar_pfull + 1, pp1, abort_flag, 6)) { ok = false; break; }
+              if (!p1_ready && !wait_one(bar_pfull + 1, pp1, abort_flag, 6)) { ok = false; break; }
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk)
@@ -455,6 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_commit(bar_sfull + 1);
               mma_commit(bar_empty + s1);  // V_{j-1}: both P.V done
               mma_commit(bar_empty + s0);  // K_j: both QK^T done
+              v_ready = mbar_test_wait(bar_full + s3, ph3);
+              p0_ready = mbar_test_wait(bar_pfull + 0, pp0 ^ 1u);
               s0 = s2;
               ph0 = ph2;
               pp0 ^= 1u;
