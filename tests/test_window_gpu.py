@@ -116,3 +116,27 @@ def test_window_workload_sampled():
     got_l = np.array([lse_c[b, h, i] for b, h, i in rows])
     compare(got_o, got_l, o_ref, lse_ref, w.name)
     assert torch.isfinite(o).all()
+
+
+@pytest.mark.parametrize("scale", [-0.11, 0.0])
+def test_window_and_cache_with_negative_or_zero_scale(scale):
+    """The general kernel instance also has a negative-scale variant (it works
+    on -s with |scale|); scale 0 gives uniform weights over each row's window."""
+    q, k, v = workloads.prefill_inputs(2, 4, 2, 300, 450, 128, seed=305)
+    for causal, window in [(0, (100, 20)), (2, (257, -1))]:
+        o, lse = _native.forward_window(q.cuda(), k.cuda(), v.cuda(), causal, window, scale)
+        assert _native.attn_get_device_status() == 0
+        o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale, window=window)
+        compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "window %s scale %g" % (window, scale))
+    lens = [450, 77]
+    _, kc, vc, L = workloads.decode_inputs(2, 4, 2, 450, 128, 0, 0, seed=306, seqlens=lens)
+    for causal in (0, 2):
+        o, lse = _native.forward_kvcache(q.cuda(), kc.cuda(), vc.cuda(), L.cuda(), causal, scale)
+        assert _native.attn_get_device_status() == 0
+        o_ref, lse_ref = oracle.attn_fwd(q, kc, vc, causal, scale, kv_len=L.numpy())
+        compare(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "kvcache scale %g causal%d" % (scale, causal))
+
+
+@pytest.mark.parametrize("window", [(63, 0), (1, 1), (300, 64)])
+def test_window_head_dim_64(window):
+    _check(2, 6, 3, 333, 333, 64, 0, window, seed=307 + window[0])
