@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libattn_sm103.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "attn.h")
 
 ATTN_OK = 0
+ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_DEVICE_ARG = 6
 STATUS_NAMES = {
     0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_MISALIGNED",
@@ -60,6 +61,8 @@ def lib():
         L.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp]
         L.attn_get_device_status.restype = i
         L.attn_get_device_status.argtypes = [vp]
+        L.attn_selftest_wait_timeout.restype = i
+        L.attn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_status_string.argtypes = [i]
         _lib = L
@@ -218,6 +221,11 @@ def attn_fwd_splitkv_noalloc(q, k_cache, v_cache, seqlens, o, lse, scale, chunk,
 
 def attn_get_device_status(stream=None):
     return lib().attn_get_device_status(_stream_handle(stream))
+
+
+def attn_selftest_wait_timeout(limit_ns, stream=None):
+    """Launches the bounded-wait self-test kernel; its timeout shows in attn_get_device_status."""
+    return lib().attn_selftest_wait_timeout(int(limit_ns), _stream_handle(stream))
 
 
 # --------------------------------------------------------------------------- convenience wrappers

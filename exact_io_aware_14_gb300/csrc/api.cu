@@ -241,13 +241,22 @@ attn_status attn_fwd_splitkv_paged(const void* q, const void* k_pages, const voi
                  o, lse, B, Hq, Hkv, d, scale, chunk, workspace, workspace_bytes, stream);
 }
 
+attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns < 1000ull) limit_ns = 1000ull;
+  if (limit_ns > 2000000000ull) limit_ns = 2000000000ull;
+  return attn::launch_selftest_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_LAUNCH;
+}
+
 attn_status attn_get_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_LAUNCH;
-  uint32_t w_prefill = 0, w_decode = 0;
+  uint32_t w_prefill = 0, w_decode = 0, w_selftest = 0;
   if (attn::fetch_status_prefill(s, &w_prefill) != cudaSuccess) return ATTN_ERR_LAUNCH;
   if (attn::fetch_status_decode(s, &w_decode) != cudaSuccess) return ATTN_ERR_LAUNCH;
-  const uint32_t w = w_prefill ? w_prefill : w_decode;
+  if (attn::fetch_status_selftest(s, &w_selftest) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  const uint32_t w = w_prefill ? w_prefill : (w_decode ? w_decode : w_selftest);
   switch (w & 0xffu) {
     case 0: return ATTN_OK;
     case attn::kDevTimeout: return ATTN_ERR_TIMEOUT;

@@ -44,5 +44,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 // then synchronises the stream).  Returns the first non-zero word, or 0.
 cudaError_t fetch_status_prefill(cudaStream_t stream, uint32_t* out);
 cudaError_t fetch_status_decode(cudaStream_t stream, uint32_t* out);
+cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+cudaError_t fetch_status_selftest(cudaStream_t stream, uint32_t* out);
 
 }  // namespace attn

@@ -57,7 +57,7 @@ struct Layout {
   static constexpr int kOffQ = 0;  // Q_0, Q_1
   static constexpr int kOffRing = kOffQ + 2 * kTile;
   static constexpr int kOffBar = kOffRing + kSlots * kTile;
-  static constexpr int kNumBars = 2 * kSlots + 6 * 2 + 1;
+  static constexpr int kNumBars = 2 * kSlots + 6 * 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_qfree = bar_qfull + 2;    // [2] last QK^T of the unit read Q_t
   uint64_t* bar_ofree = bar_qfree + 2;    // [2] epilogue read O_t out of TMEM (4 softmax warps)
   uint64_t* bar_vfix = bar_ofree + 2;     // last V tile of a cache row landed (producer only)
+  uint64_t* bar_drain = bar_vfix + 1;     // after an abort: the MMAs issued so far completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
 
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_ofree + t, 4);
     }
     mbar_init(bar_vfix, 1);
+    mbar_init(bar_drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -322,6 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       uint32_t item_base = 0, vfix_uses = 0;
+      uint32_t issued = 0;         // ring items issued so far
+      int q_issued[2] = {0, 0};    // Q loads issued per tile
+      bool vfix_pending = false;   // the last item's load completes on bar_vfix and was not awaited
       int uc = 0;
       bool ok = true;
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
@@ -336,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < D / 64; ++h)
             tma_load_4d(sQ + t * L::kTile + h * L::kHalf, &tm_q, bar_qfull + t, h * 64, u.ti[t].hq, u.ti[t].row0,
                         u.b);
+          q_issued[t] = uc + 1;
         }
         for (int item = 0; ok && item < 2 * u.n_kt; ++item) {
           const uint32_t gi = item_base + item;
@@ -355,8 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < D / 64; ++h)
             tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, done, h * 64, u.hkv,
                         (u.kt0 + kt) * BN, u.b);
+          issued = gi + 1;
           if (fix) {
-            if (!wait_one(bar_vfix, vfix_uses & 1, abort_flag, 12)) { ok = false; break; }
+            if (!wait_one(bar_vfix, vfix_uses & 1, abort_flag, 12)) {
+              vfix_pending = true;
+              ok = false;
+              break;
+            }
             ++vfix_uses;
             for (int h = 0; h < D / 64; ++h) {
               uint8_t* base = sRing + slot * L::kTile + h * L::kHalf;
@@ -369,6 +380,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         item_base += 2 * u.n_kt;
         ++uc;
+      }
+      if (!ok) {
+        // after an abort, loads already issued may still be in flight: they
+        // land before the CTA may exit (bounded, not abortable).  Only the
+        // last item of each ring slot can be pending.
+        volatile int no_abort = 0;
+        for (int t = 0; t < 2; ++t)
+          if (q_issued[t] > 0) mbar_wait(bar_qfull + t, (q_issued[t] - 1) & 1, &no_abort, kWaitLimitNs);
+        for (int s = 0; s < NS && static_cast<uint32_t>(s) < issued; ++s) {
+          const uint32_t last = s + NS * ((issued - 1 - s) / NS);
+          if (vfix_pending && last == issued - 1) continue;  // completes on bar_vfix instead
+          mbar_wait(bar_full + s, (last / NS) & 1, &no_abort, kWaitLimitNs);
+        }
+        if (vfix_pending) mbar_wait(bar_vfix, vfix_uses & 1, &no_abort, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -533,6 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         kc[1] += u.ti[1].n_kt;
         item_base += 2 * n_kt;
         ++uc;
+      }
+      if (!ok) {
+        // after an abort, the MMAs issued so far complete before TMEM is freed
+        volatile int no_abort = 0;
+        mma_commit(bar_drain);
+        mbar_wait(bar_drain, 0, &no_abort, kWaitLimitNs);
       }
     }
   } else if (warp >= 4) {

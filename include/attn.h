@@ -231,6 +231,22 @@ ATTN_API attn_status attn_fwd_splitkv_noalloc(const void* q, const void* k_cache
  */
 ATTN_API attn_status attn_get_device_status(void* stream);
 
+/*
+ * Self-test of failure detection.  Every wait of the library's kernels on a
+ * pipeline barrier is bounded: when it runs out (2 s) the kernel records
+ * ATTN_ERR_TIMEOUT, lets its in-flight copies and tensor-core work finish,
+ * frees its Tensor Memory and returns, instead of hanging.  This call
+ * launches one small kernel on `stream` whose waits can never be satisfied
+ * (barriers that nothing completes): one warp gives up after limit_ns
+ * (clamped to [1 us, 2 s]) and the other, with the full limit, must give up
+ * as soon as it sees the first one's abort.  Afterwards
+ * attn_get_device_status returns ATTN_ERR_TIMEOUT once and the context is
+ * usable.  Returns ATTN_OK when the kernel was launched.  The pages have no
+ * counterpart to this call; it exists so that the timeout path can be
+ * tested without a GPU fault.
+ */
+ATTN_API attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 ATTN_API const char* attn_status_string(attn_status s);
 
