@@ -157,7 +157,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   using L = DLayout<D>;
   constexpr int NCH = D / 64;  // 16-byte chunks per key that one score thread reads
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base (TMA's 128-byte swizzle), taken as an offset into
+  // the shared array itself: pointers derived from it stay in the shared
+  // space, so the compiler emits shared loads and stores and needs no
+  // generic-to-shared conversion for every barrier operation
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   // grid (KV head x head block, batch, split).  Up to kRankB sequences the
   // CTA with linear item index (z, y) takes the item pick_item lists there;

@@ -268,7 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NS = L::kSlots;
   const int* const lens = kGeneral ? seqlens : nullptr;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base (TMA's 128-byte swizzle), taken as an offset into
+  // the shared array itself: pointers derived from it stay in the shared
+  // space, so the compiler emits shared loads and stores and needs no
+  // generic-to-shared conversion for every barrier operation
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* bar_full = bars;              // [NS] ring slot loaded
