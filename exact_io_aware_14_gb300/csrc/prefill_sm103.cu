@@ -101,32 +101,75 @@ struct TileInfo {
 // of range, and O / l and the LSE come out the same.
 constexpr float kRescaleLog2 = 8.f;
 
-// Row max of one 128-column score tile in TMEM (this thread's lane), read in
-// two 64-column halves.  kNeg: the scale is negative, work on -s.
-// Masked tiles keep columns [lo, lim) (kLo) or [0, lim).
+// One 64-column half h of this lane's scores, read from TMEM.  Masked tiles
+// keep columns [lo, lim) (kLo) or [0, lim); kNeg: the scale is negative and
+// the kernel works on -s.
+__device__ __forceinline__ void load_half(uint32_t tS, int h, uint32_t (&u)[2][32]) {
+  tmem_ld32(tS + 64 * h, u[0]);
+  tmem_ld32(tS + 64 * h + 32, u[1]);
+  tmem_wait_ld();
+}
+
+template <bool kMasked, bool kNeg, bool kLo>
+__device__ __forceinline__ float half_max(const uint32_t (&u)[2][32], int h, int lo, int lim) {
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 64; i += 4) {
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = __uint_as_float(u[(i + k) >> 5][(i + k) & 31]);
+      if (kNeg) v[k] = -v[k];
+      if (kMasked) v[k] = (64 * h + i + k < lim && (!kLo || 64 * h + i + k >= lo)) ? v[k] : -INFINITY;
+    }
+    mx0 = fmax3(mx0, v[0], v[1]);
+    mx1 = fmax3(mx1, v[2], v[3]);
+  }
+  return fmaxf(mx0, mx1);
+}
+
+// p = 2^(s*c - mc) for half h, packed as bf16 pairs into pk and summed into
+// acc0 / acc1.
+template <bool kMasked, bool kNeg, bool kLo>
+__device__ __forceinline__ void half_exp(const uint32_t (&u)[2][32], int h, int lo, int lim, float c, float mc,
+                                         float2& acc0, float2& acc1, uint32_t (&pk)[32]) {
+  const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float v0 = __uint_as_float(u[i >> 4][(2 * i) & 31]);
+    float v1 = __uint_as_float(u[i >> 4][(2 * i + 1) & 31]);
+    if (kNeg) {
+      v0 = -v0;
+      v1 = -v1;
+    }
+    const float2 x = ffma2(make_float2(v0, v1), c2, nmc2);
+    float p0 = ex2_approx(x.x);
+    float p1 = ex2_approx(x.y);
+    if (kMasked) {  // also right for c == 0, where -inf * 0 would not give 0
+      p0 = (64 * h + 2 * i < lim && (!kLo || 64 * h + 2 * i >= lo)) ? p0 : 0.f;
+      p1 = (64 * h + 2 * i + 1 < lim && (!kLo || 64 * h + 2 * i + 1 >= lo)) ? p1 : 0.f;
+    }
+    if (i & 1)
+      acc1 = fadd2(acc1, make_float2(p0, p1));
+    else
+      acc0 = fadd2(acc0, make_float2(p0, p1));
+    pk[i] = pack_bf16x2(p0, p1);
+  }
+}
+
+__device__ __forceinline__ float acc_sum(float2 a0, float2 a1) { return (a0.x + a0.y) + (a1.x + a1.y); }
+
+// Row max of one 128-column score tile (this thread's lane).
 template <bool kMasked, bool kNeg, bool kLo = false>
 __device__ __forceinline__ float score_tile_max(uint32_t tS, int lo, int lim) {
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+  float mx = -INFINITY;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t u[2][32];
-    tmem_ld32(tS + 64 * h, u[0]);
-    tmem_ld32(tS + 64 * h + 32, u[1]);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 64; i += 4) {
-      float v[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[k] = __uint_as_float(u[(i + k) >> 5][(i + k) & 31]);
-        if (kNeg) v[k] = -v[k];
-        if (kMasked) v[k] = (64 * h + i + k < lim && (!kLo || 64 * h + i + k >= lo)) ? v[k] : -INFINITY;
-      }
-      mx0 = fmax3(mx0, v[0], v[1]);
-      mx1 = fmax3(mx1, v[2], v[3]);
-    }
+    load_half(tS, h, u);
+    mx = fmaxf(mx, half_max<kMasked, kNeg, kLo>(u, h, lo, lim));
   }
-  return fmaxf(mx0, mx1);
+  return mx;
 }
 
 // p = 2^(s*c - mc) for the 128 scores of this lane, written back as bf16
@@ -135,38 +178,112 @@ __device__ __forceinline__ float score_tile_max(uint32_t tS, int lo, int lim) {
 template <bool kMasked, bool kNeg, bool kLo = false>
 __device__ __forceinline__ float score_tile_exp(uint32_t tS, int lo, int lim, float c, float mc) {
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-  const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
 #pragma unroll 1
   for (int h = 0; h < 2; ++h) {
-    uint32_t u[2][32];
-    tmem_ld32(tS + 64 * h, u[0]);
-    tmem_ld32(tS + 64 * h + 32, u[1]);
-    tmem_wait_ld();
-    uint32_t pk[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float v0 = __uint_as_float(u[i >> 4][(2 * i) & 31]);
-      float v1 = __uint_as_float(u[i >> 4][(2 * i + 1) & 31]);
-      if (kNeg) {
-        v0 = -v0;
-        v1 = -v1;
-      }
-      const float2 x = ffma2(make_float2(v0, v1), c2, nmc2);
-      float p0 = ex2_approx(x.x);
-      float p1 = ex2_approx(x.y);
-      if (kMasked) {  // also right for c == 0, where -inf * 0 would not give 0
-        p0 = (64 * h + 2 * i < lim && (!kLo || 64 * h + 2 * i >= lo)) ? p0 : 0.f;
-        p1 = (64 * h + 2 * i + 1 < lim && (!kLo || 64 * h + 2 * i + 1 >= lo)) ? p1 : 0.f;
-      }
-      if (i & 1)
-        acc1 = fadd2(acc1, make_float2(p0, p1));
-      else
-        acc0 = fadd2(acc0, make_float2(p0, p1));
-      pk[i] = pack_bf16x2(p0, p1);
-    }
+    uint32_t u[2][32], pk[32];
+    load_half(tS, h, u);
+    half_exp<kMasked, kNeg, kLo>(u, h, lo, lim, c, mc, acc0, acc1, pk);
     tmem_st32(tS + 32 * h, pk);
   }
-  return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+  return acc_sum(acc0, acc1);
+}
+
+// A half's p sum above this means one of its p passed it; below it every
+// p <= 2^16, which bf16 P and the fp32 row sum and O accumulator hold with
+// full relative precision.
+constexpr float kSumLimit = 65536.f;
+
+struct HalfFix {
+  float sum;  // the half's (or the tile's) row sum after the fix
+  float m;    // the lane's exponent reference after the fix
+};
+
+// Rare path of the one-pass softmax, half 0: some lane's half-0 sum passed
+// kSumLimit (flag ov) before its P was stored, so its scores are still in
+// TMEM.  Every lane of the warp calls this together (TMEM accesses are
+// warp-wide); a lane with ov moves its reference to the half's max, the
+// others recompute the same P.  Stores half 0's P.
+template <bool kMasked, bool kNeg, bool kLo>
+__device__ __noinline__ HalfFix fix_half0(uint32_t tS, int lo, int lim, float c, float m, bool ov) {
+  uint32_t u[2][32], pk[32];
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  load_half(tS, 0, u);
+  if (ov) m = fmaxf(m, half_max<kMasked, kNeg, kLo>(u, 0, lo, lim));
+  half_exp<kMasked, kNeg, kLo>(u, 0, lo, lim, c, m * c, a0, a1, pk);
+  tmem_st32(tS, pk);
+  return {acc_sum(a0, a1), m};
+}
+
+// Rare path, half 1: some lane's half-1 sum passed kSumLimit; half 1's
+// scores are still in TMEM, half 0's P went out under the reference m.  A
+// lane with ov moves its reference to the half's max and rescales its stored
+// half-0 P (and sum t0) by 2^(m*c - m_new*c); every lane recomputes and
+// stores half 1's P.  Returns the tile's row sum.
+template <bool kMasked, bool kNeg, bool kLo>
+__device__ __noinline__ HalfFix fix_half1(uint32_t tS, int lo, int lim, float c, float m, float t0, bool ov) {
+  uint32_t u[2][32], pk[32];
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  load_half(tS, 1, u);
+  float a01 = 1.f;
+  if (ov) {
+    const float m_new = fmaxf(m, half_max<kMasked, kNeg, kLo>(u, 1, lo, lim));
+    a01 = ex2_approx(m * c - m_new * c);
+    m = m_new;
+  }
+  half_exp<kMasked, kNeg, kLo>(u, 1, lo, lim, c, m * c, a0, a1, pk);
+  tmem_st32(tS + 32, pk);
+  tmem_wait_st();  // half 0's P was stored by the caller just before
+  tmem_ld32(tS, u[0]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float lo_f = __uint_as_float(u[0][i] << 16), hi_f = __uint_as_float(u[0][i] & 0xffff0000u);
+    u[0][i] = (a01 != 1.f) ? pack_bf16x2(lo_f * a01, hi_f * a01) : u[0][i];
+  }
+  tmem_st32(tS, u[0]);
+  return {t0 * a01 + acc_sum(a0, a1), m};
+}
+
+// One pass over the tile for rows whose exponent reference m is set (every
+// row of the warp has seen scores): p = 2^(s*c - m*c) under the current
+// reference, each score read once and no max formed; a half whose p sum
+// passes kSumLimit sends the warp through fix_half0 / fix_half1, which move
+// that row's reference.  Keeps the two-pass form's summation order, so the
+// result is the same whenever the reference does not move.  Returns the row
+// sum in units of the updated reference m.
+template <bool kMasked, bool kNeg, bool kLo = false>
+__device__ __forceinline__ float score_tile_onepass(uint32_t tS, int lo, int lim, float c, float& m) {
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+  uint32_t u[2][32], pk[32];
+  load_half(tS, 0, u);
+  half_exp<kMasked, kNeg, kLo>(u, 0, lo, lim, c, m * c, acc0, acc1, pk);
+  float t0 = acc_sum(acc0, acc1);
+  const bool ov0 = !(t0 <= kSumLimit);
+  if (__any_sync(0xffffffffu, ov0)) {
+    const HalfFix f = fix_half0<kMasked, kNeg, kLo>(tS, lo, lim, c, m, ov0);
+    if (ov0) {
+      m = f.m;
+      t0 = f.sum;
+      acc0 = make_float2(t0, 0.f);  // later sums build on the fixed half-0 sum
+      acc1 = make_float2(0.f, 0.f);
+    }
+  } else {
+    tmem_st32(tS, pk);
+  }
+  load_half(tS, 1, u);
+  half_exp<kMasked, kNeg, kLo>(u, 1, lo, lim, c, m * c, acc0, acc1, pk);
+  float total = acc_sum(acc0, acc1);
+  const bool ov1 = !(total - t0 <= kSumLimit);
+  if (__any_sync(0xffffffffu, ov1)) {
+    const HalfFix f = fix_half1<kMasked, kNeg, kLo>(tS, lo, lim, c, m, t0, ov1);
+    if (ov1) {
+      m = f.m;
+      total = f.sum;
+    }
+  } else {
+    tmem_st32(tS + 32, pk);
+  }
+  return total;
 }
 
 // Work unit U -> (batch, KV head, the two query tiles).  Units are numbered
@@ -612,17 +729,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (causal) lim = min(lim, grow + u.coff - kbase + 1);
           }
         }
-        const float mt = masked ? score_tile_max<true, kNeg, kGeneral>(tS, lo, lim)
-                                : score_tile_max<false, kNeg>(tS, lo, lim);
-        // move the reference only on the first visible scores or when the tile
-        // max is more than 2^kRescaleLog2 above it
-        const bool need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
-        const float m_new = need ? fmaxf(m, mt) : m;
-        const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
-        const float alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
-        const float rowsum = masked ? score_tile_exp<true, kNeg, kGeneral>(tS, lo, lim, c, mc)
-                                    : score_tile_exp<false, kNeg>(tS, lo, lim, c, mc);
-        l = l * alpha + rowsum;
+        bool need;
+        float m_new, alpha;
+        if (__any_sync(0xffffffffu, m == -INFINITY)) {
+          // some row of the warp sees its first scores: the tile max sets the
+          // reference, which then moves only when a tile max is more than
+          // 2^kRescaleLog2 above it
+          const float mt = masked ? score_tile_max<true, kNeg, kGeneral>(tS, lo, lim)
+                                  : score_tile_max<false, kNeg>(tS, lo, lim);
+          need = (m == -INFINITY) || ((mt - m) * c > kRescaleLog2);
+          m_new = need ? fmaxf(m, mt) : m;
+          const float mc = (m_new == -INFINITY) ? 0.f : m_new * c;
+          alpha = (m == -INFINITY) ? 0.f : (need ? ex2_approx(fmaf(m, c, -mc)) : 1.f);
+          const float rowsum = masked ? score_tile_exp<true, kNeg, kGeneral>(tS, lo, lim, c, mc)
+                                      : score_tile_exp<false, kNeg>(tS, lo, lim, c, mc);
+          l = l * alpha + rowsum;
+        } else {
+          // no max between the scores and the exponentials on the path to P
+          m_new = m;
+          const float rowsum = masked ? score_tile_onepass<true, kNeg, kGeneral>(tS, lo, lim, c, m_new)
+                                      : score_tile_onepass<false, kNeg>(tS, lo, lim, c, m_new);
+          need = m_new != m;
+          alpha = need ? ex2_approx(fmaf(m, c, -m_new * c)) : 1.f;
+          l = l * alpha + rowsum;
+        }
 
         // O_t holds the sum through tile j-1 (P.V of j-1 completed before S_j was
         // written): rescale it now if this row's reference moved.
