@@ -43,6 +43,15 @@ def test_group_sizes_and_head_dims(Hq, Hkv, d):
     _check(q, k, v, L, d ** -0.5, 1024, "Hq%d Hkv%d d%d" % (Hq, Hkv, d))
 
 
+def test_lengths_at_the_workload_maximum():
+    """Lengths at the workload's top (16384: sixteen full 1024-key splits) and
+    right around it and its lowest length, in the workload's configuration."""
+    w = workloads.DECODE
+    lens = [16384, 16383, 15361, 1024, 1025, 16384]
+    q, k, v, L = workloads.decode_inputs(len(lens), w.Hq, w.Hkv, w.max_seqlen, w.d, 0, 0, seed=48, seqlens=lens)
+    _check(q, k, v, L, w.scale, w.chunk, "lengths at 16384")
+
+
 @pytest.mark.parametrize("chunk", [64, 256, 1024, 4096])
 def test_chunk_sizes(chunk):
     lens = [5, 700, 4096, 4000]
