@@ -15,10 +15,12 @@
 //                 after the last MMA that reads a ring slot frees it.
 //   warps 4-7     softmax of tile 0, warps 8-11 softmax of tile 1: one
 //                 thread owns one query row (one TMEM lane); it reads its
-//                 128 scores, updates the running max m and sum l, rescales
-//                 its O row in TMEM only if m moved, and writes P (bf16)
-//                 back into TMEM over the scores; the P.V MMA reads P from
-//                 TMEM as its A operand.  At the end: O / l and the LSE.
+//                 128 scores, forms p under the row's exponent reference m
+//                 (taking the tile max only where m is first set or must
+//                 move), adds to the sum l, rescales its O row in TMEM only
+//                 if m moved, and writes P (bf16) back into TMEM over the
+//                 scores; the P.V MMA reads P from TMEM as its A operand.
+//                 At the end: O / l and the LSE.
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
 // O_1 [384,384+d); P_t is packed bf16x2 in the first 64 columns of S_t.
@@ -95,10 +97,12 @@ struct TileInfo {
   int n_kt;  // key tiles this tile visits (0: inactive)
 };
 
-// The exponent reference of a row is moved (and O, l rescaled) only when the
-// tile max exceeds it by more than this many powers of two; until then p may
-// reach 2^8, which bf16 P, fp32 l and the fp32 O accumulator hold without loss
-// of range, and O / l and the LSE come out the same.
+// Where a tile's max is taken (a row's first visible scores, or a warp's rare
+// fix-up), the row's exponent reference is moved (and O, l rescaled) only when
+// that max exceeds it by more than this many powers of two.  Between moves p
+// stays small enough (2^8 here, 2^16 under the one-pass form's sum check
+// below) for bf16 P, fp32 l and the fp32 O accumulator to hold it with full
+// relative precision, and O / l and the LSE come out the same.
 constexpr float kRescaleLog2 = 8.f;
 
 // One 64-column half h of this lane's scores, read from TMEM.  Masked tiles
