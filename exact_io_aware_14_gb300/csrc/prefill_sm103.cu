@@ -299,10 +299,12 @@ __device__ __forceinline__ float score_tile_onepass(uint32_t tS, int lo, int lim
 // bottom-right (coff = nk - Nq); a local window (wl, wr) is aligned
 // bottom-right: row i sits at key position i + nk - Nq and sees wl keys
 // before it and wr after it (negative: that side unbounded).  The unit's key
-// tiles are kt0 .. kt0 + n_kt - 1; tile t visits the first ti[t].n_kt of them.
+// tiles are kt0 .. kt0 + n_kt - 1; tile t visits the first ti[t].n_kt of them
+// in the order key_tile gives.
 struct Unit {
   int b, hkv, n_kt;
   int nk, coff, lo, kt0;
+  bool rot;  // visit kt0 last (key_tile)
   TileInfo ti[2];
 };
 template <bool kGeneral>
@@ -332,6 +334,7 @@ __device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int N
     u.coff = (causal == 2) ? u.nk - Nq : 0;
     u.lo = 0;
     u.kt0 = 0;
+    u.rot = false;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int kend = causal ? max(0, min(u.nk, u.ti[t].row0 + BM + u.coff)) : u.nk;
@@ -358,9 +361,26 @@ __device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int N
     u.kt0 = first / BN;
 #pragma unroll
     for (int t = 0; t < 2; ++t) u.ti[t].n_kt = kend[t] > 0 ? (kend[t] + BN - 1) / BN - u.kt0 : 0;
+    // Under a left window bound the first key tile is usually a staircase
+    // that some rows see only in part.  A row's first visited tile is the one
+    // where its max is taken in two passes, which on a masked tile costs about
+    // twice an unmasked one and sits on the critical path of the unit's start;
+    // when both query tiles visit the same key tiles (a head pair) and a full
+    // tile follows, kt0 is visited last instead.  Visiting order does not
+    // change what is computed, only the rounding order of the sums.
+    u.rot = pair_heads && u.ti[0].n_kt >= 3 && u.ti[1].n_kt == u.ti[0].n_kt &&
+            u.kt0 * BN < u.ti[0].row0 + BM - 1 + u.lo;
   }
   u.n_kt = max(u.ti[0].n_kt, u.ti[1].n_kt);
   return u;
+}
+
+// Key tile visited at step j of a unit: kt0 + j, or with u.rot kt0 + 1,
+// kt0 + 2, ..., kt0 + n_kt - 1 and then kt0.
+template <bool kGeneral>
+__device__ __forceinline__ int key_tile(const Unit& u, int j) {
+  if (!kGeneral) return j;  // kt0 = 0, no rotation
+  return u.kt0 + (u.rot ? (j + 1 < u.n_kt ? j + 1 : 0) : j);
 }
 
 // Unit of round r for this CTA: zig-zag over the CTAs (c, then G-1-c, ...),
@@ -479,13 +499,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // hold anything, NaN included (and P = 0 times NaN is not 0): it is
           // loaded against a private barrier and those rows are cleared before
           // the MMA thread is told the tile is there.
-          const int valid = u.nk - (u.kt0 + kt) * BN;
+          const int ktile = key_tile<kGeneral>(u, kt);
+          const int valid = u.nk - ktile * BN;
           const bool fix = kGeneral && lens && is_v && valid < BN;
           uint64_t* done = fix ? bar_vfix : bar_full + slot;
           mbar_arrive_expect_tx(done, L::kTile);
           for (int h = 0; h < D / 64; ++h)
             tma_load_4d(sRing + slot * L::kTile + h * L::kHalf, is_v ? &tm_v : &tm_k, done, h * 64, u.hkv,
-                        (u.kt0 + kt) * BN, u.b);
+                        ktile * BN, u.b);
           issued = gi + 1;
           if (fix) {
             if (!wait_one(bar_vfix, vfix_uses & 1, abort_flag, 12)) {
@@ -717,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < my_kt; ++j) {
         if (!wait_all(bar_sfull + t, (kc + j) & 1, abort_flag, 7)) { ok = false; break; }
         tc_fence_after();
-        const int kbase = (u.kt0 + j) * BN;
+        const int kbase = key_tile<kGeneral>(u, j) * BN;
         bool masked;
         int lim = BN, lo = 0;  // columns outside [lo, lim) of this tile are masked for this row
         if (kGeneral) {

@@ -7,7 +7,9 @@ position i + L - Nq and sees keys from position - left to position + right
 example passes causal with window (1023, 0)).  Shapes span several tiles
 with ragged tails, both ways of pairing query tiles in a CTA (GQA head
 pairs, consecutive row tiles of one head), more units than SMs, windows
-narrower than a tile, one-sided windows and rows whose window holds no key.
+narrower than a tile, one-sided windows, rows whose window holds no key, and
+head pairs whose left-edge key tile is visited last (also against a cache
+whose last V tile runs past the cache length).
 """
 import math
 
@@ -57,6 +59,7 @@ def _check(B, Hq, Hkv, Nq, Nk, d, causal, window, seed):
     (2, 96, 32, 130, 390, 128, 0, (17, 5)),      # group size 3
     (2, 2, 2, 1, 517, 128, 0, (100, 0)),         # one query row: the last 101 keys
     (1, 2, 2, 1000, 1000, 64, 0, (500, 500)),
+    (2, 8, 2, 600, 600, 64, 1, (383, 0)),        # head pairs whose left-edge key tile is visited last
 ])
 def test_window_parity(B, Hq, Hkv, Nq, Nk, d, causal, window):
     _check(B, Hq, Hkv, Nq, Nk, d, causal, window, seed=300 + Nq + Nk)
@@ -84,7 +87,7 @@ def test_window_covering_everything_equals_attn_fwd_bitwise():
     assert torch.equal(c[0], e[0]) and torch.equal(c[1], e[1])
 
 
-@pytest.mark.parametrize("causal,window", [(2, (100, 0)), (0, (40, 40)), (1, (300, -1))])
+@pytest.mark.parametrize("causal,window", [(2, (100, 0)), (0, (40, 40)), (1, (300, -1)), (2, (300, 0))])
 def test_kvcache_with_window(causal, window):
     """A query block against a cache with per-sequence lengths and a window
     (positions taken with L = the sequence's cache length); cache positions
