@@ -163,6 +163,36 @@ __device__ __forceinline__ void half_exp(const uint32_t (&u)[2][32], int h, int 
 
 __device__ __forceinline__ float acc_sum(float2 a0, float2 a1) { return (a0.x + a0.y) + (a1.x + a1.y); }
 
+// half_exp for one 32-column quarter q of the scores (uq: its raw values),
+// writing pairs (q & 1) * 16 .. + 15 of the half's packed P.  Two quarters in
+// order give the same operations in the same order as half_exp.
+template <bool kMasked, bool kNeg, bool kLo>
+__device__ __forceinline__ void quarter_exp(const uint32_t (&uq)[32], int q, int lo, int lim, float c, float mc,
+                                            float2& acc0, float2& acc1, uint32_t (&pk)[32]) {
+  const float2 c2 = make_float2(c, c), nmc2 = make_float2(-mc, -mc);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float v0 = __uint_as_float(uq[2 * i]);
+    float v1 = __uint_as_float(uq[2 * i + 1]);
+    if (kNeg) {
+      v0 = -v0;
+      v1 = -v1;
+    }
+    const float2 x = ffma2(make_float2(v0, v1), c2, nmc2);
+    float p0 = ex2_approx(x.x);
+    float p1 = ex2_approx(x.y);
+    if (kMasked) {
+      p0 = (32 * q + 2 * i < lim && (!kLo || 32 * q + 2 * i >= lo)) ? p0 : 0.f;
+      p1 = (32 * q + 2 * i + 1 < lim && (!kLo || 32 * q + 2 * i + 1 >= lo)) ? p1 : 0.f;
+    }
+    if (i & 1)
+      acc1 = fadd2(acc1, make_float2(p0, p1));
+    else
+      acc0 = fadd2(acc0, make_float2(p0, p1));
+    pk[(q & 1) * 16 + i] = pack_bf16x2(p0, p1);
+  }
+}
+
 // Row max of one 128-column score tile (this thread's lane).
 template <bool kMasked, bool kNeg, bool kLo = false>
 __device__ __forceinline__ float score_tile_max(uint32_t tS, int lo, int lim) {
@@ -258,9 +288,18 @@ __device__ __noinline__ HalfFix fix_half1(uint32_t tS, int lo, int lim, float c,
 template <bool kMasked, bool kNeg, bool kLo = false>
 __device__ __forceinline__ float score_tile_onepass(uint32_t tS, int lo, int lim, float c, float& m) {
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-  uint32_t u[2][32], pk[32];
-  load_half(tS, 0, u);
-  half_exp<kMasked, kNeg, kLo>(u, 0, lo, lim, c, m * c, acc0, acc1, pk);
+  uint32_t ua[32], ub[32], pk[32];
+  // each quarter's load is issued before the previous quarter's arithmetic
+  // and awaited after it; no call and no use of a register in flight comes
+  // between a load and its wait
+  tmem_ld32(tS, ua);
+  tmem_wait_ld();
+  tmem_ld32(tS + 32, ub);
+  quarter_exp<kMasked, kNeg, kLo>(ua, 0, lo, lim, c, m * c, acc0, acc1, pk);
+  tmem_wait_ld();
+  tmem_ld32(tS + 64, ua);
+  quarter_exp<kMasked, kNeg, kLo>(ub, 1, lo, lim, c, m * c, acc0, acc1, pk);
+  tmem_wait_ld();
   float t0 = acc_sum(acc0, acc1);
   const bool ov0 = !(t0 <= kSumLimit);
   if (__any_sync(0xffffffffu, ov0)) {
@@ -274,8 +313,10 @@ __device__ __forceinline__ float score_tile_onepass(uint32_t tS, int lo, int lim
   } else {
     tmem_st32(tS, pk);
   }
-  load_half(tS, 1, u);
-  half_exp<kMasked, kNeg, kLo>(u, 1, lo, lim, c, m * c, acc0, acc1, pk);
+  tmem_ld32(tS + 96, ub);
+  quarter_exp<kMasked, kNeg, kLo>(ua, 2, lo, lim, c, m * c, acc0, acc1, pk);
+  tmem_wait_ld();
+  quarter_exp<kMasked, kNeg, kLo>(ub, 3, lo, lim, c, m * c, acc0, acc1, pk);
   float total = acc_sum(acc0, acc1);
   const bool ov1 = !(total - t0 <= kSumLimit);
   if (__any_sync(0xffffffffu, ov1)) {
