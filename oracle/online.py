@@ -39,9 +39,23 @@ def _visible(nq, nk, causal, kv_len):
     return vis
 
 
+def _tile_starts(nk, tile, tile_order):
+    starts = list(range(0, nk, tile))
+    if tile_order is None:
+        return starts
+    assert sorted(tile_order) == list(range(len(starts))), "tile_order must be a permutation of the tiles"
+    return [starts[t] for t in tile_order]
+
+
 def online_attention(q, k, v, scale, causal=False, tile=64, kv_len=None,
-                     conditional_rescale=True, normalise_each_tile=False, rescale_threshold=None):
+                     conditional_rescale=True, normalise_each_tile=False, rescale_threshold=None,
+                     tile_order=None):
     """Tiled online softmax over key tiles of ``tile`` keys. Returns (O, LSE).
+
+    ``tile_order``: the order in which the key tiles are visited (a
+    permutation of their indices; default ascending).  The running state
+    (m, l, a) only ever takes a max and rescaled sums, so any order reaches
+    the same result up to rounding.
 
     ``rescale_threshold`` (natural-log units): when given, the exponent
     reference m of a row is moved -- and l, a rescaled -- only when a tile's
@@ -50,14 +64,14 @@ def online_attention(q, k, v, scale, causal=False, tile=64, kv_len=None,
     a bounded range); otherwise the stale reference is kept and p may exceed 1.
     """
     if rescale_threshold is not None:
-        return _online_thresholded(q, k, v, scale, causal, tile, kv_len, rescale_threshold)
+        return _online_thresholded(q, k, v, scale, causal, tile, kv_len, rescale_threshold, tile_order)
     nq, d = q.shape
     nk = k.shape[0]
     vis = _visible(nq, nk, causal, kv_len)
     m = np.full(nq, -np.inf)
     l = np.zeros(nq)
     a = np.zeros((nq, v.shape[1]))
-    for j0 in range(0, nk, tile):
+    for j0 in _tile_starts(nk, tile, tile_order):
         j1 = min(nk, j0 + tile)
         s = scale * (q @ k[j0:j1].T)                      # score tile
         s = np.where(vis[:, j0:j1], s, -np.inf)
@@ -90,14 +104,14 @@ def online_attention(q, k, v, scale, causal=False, tile=64, kv_len=None,
     return o, lse
 
 
-def _online_thresholded(q, k, v, scale, causal, tile, kv_len, threshold):
+def _online_thresholded(q, k, v, scale, causal, tile, kv_len, threshold, tile_order=None):
     nq = q.shape[0]
     nk = k.shape[0]
     vis = _visible(nq, nk, causal, kv_len)
     m = np.full(nq, -np.inf)          # exponent reference (may lag the true max)
     l = np.zeros(nq)
     a = np.zeros((nq, v.shape[1]))
-    for j0 in range(0, nk, tile):
+    for j0 in _tile_starts(nk, tile, tile_order):
         j1 = min(nk, j0 + tile)
         s = scale * (q @ k[j0:j1].T)
         s = np.where(vis[:, j0:j1], s, -np.inf)

@@ -101,3 +101,31 @@ def test_combine_ignores_empty_splits():
     a, b = online.combine(o_s, lse_s), online.combine(o_s2, lse_s2)
     np.testing.assert_allclose(a[0], b[0], rtol=0, atol=1e-15)
     np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("order", ["edge_last", "reversed", "shuffled"])
+@pytest.mark.parametrize("threshold", [None, 8 * math.log(2)])
+def test_any_tile_order_matches_naive(order, threshold):
+    """A unit's key tiles may be visited in another order (the prefill kernel
+    visits a window's left-edge tile last): the running state only takes
+    maxima and rescaled sums, so every order reaches the naive result, also
+    for rows that see nothing in the first tiles visited (causal rows of the
+    first tile when it comes last) and with a cache length."""
+    Nq, Nk, d, tile = 40, 70, 16, 16  # five key tiles, the last one ragged
+    q, k, v = _rand(Nq, Nk, d, seed=77)
+    n = -(-Nk // tile)
+    orders = {"edge_last": list(range(1, n)) + [0], "reversed": list(range(n))[::-1],
+              "shuffled": [int(t) for t in np.random.default_rng(3).permutation(n)]}
+    for causal in (False, True):
+        for L in (Nk, 53):
+            o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 0.3, kv_len=[L])
+            o, lse = online.online_attention(_head(q), _head(k), _head(v), 0.3, causal, tile, kv_len=L,
+                                             rescale_threshold=threshold, tile_order=orders[order])
+            np.testing.assert_allclose(o, o_ref[0, :, 0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse, lse_ref[0, 0], rtol=0, atol=1e-12)
+
+
+def test_tile_order_must_be_a_permutation():
+    q, k, v = _rand(4, 40, 8, seed=78)
+    with pytest.raises(AssertionError):
+        online.online_attention(_head(q), _head(k), _head(v), 0.3, tile=16, tile_order=[0, 0, 1])
