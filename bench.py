@@ -213,12 +213,17 @@ def oracle_sample_rate(w, q, k, v, seqlens, budget_s, seed):
         work, dt, _ = run(n)
     n_target = int(min(w.B * w.Hq * Nq, max(n, n * budget_s / max(dt, 1e-6))))
     work, dt, nrows = run(n_target)
+    whole = nrows >= w.B * w.Hq * Nq
     if dec:
         value = work / dt / 1e9
-        desc = "%d seeded (b, hq) rows of the decode workload, all valid keys each (%.1f s)" % (nrows, dt)
+        desc = "%s%d seeded (b, hq) rows of the decode workload, all valid keys each (%.1f s)" % (
+            "all " if whole else "", nrows, dt)
     else:
         value = work / dt / 1e12
-        desc = "%d seeded query rows of the workload, every visible key (%.1f s)" % (nrows, dt)
+        desc = "%s%d seeded query rows of the workload, every visible key (%.1f s)" % (
+            "all " if whole else "", nrows, dt)
+    if whole:
+        desc += ": the whole workload"
     return value, dt, desc, threads
 
 
