@@ -52,7 +52,7 @@ def bf16(rng, shape, amp):
     return torch.from_numpy(rng.standard_normal(shape) * amp).to(torch.bfloat16)
 
 
-@settings(max_examples=120, deadline=None)
+@settings(max_examples=120, deadline=None, derandomize=True)
 @given(B=st.integers(1, 2), G=st.sampled_from([1, 2, 3]), Hkv=st.integers(1, 2), Nq=st.integers(1, 40),
        Nk=st.integers(1, 40), d=st.sampled_from([4, 8, 16]), causal=st.sampled_from([0, 1, 2]),
        window=st.one_of(st.none(), st.tuples(st.integers(-1, 45), st.integers(-1, 45))),
@@ -82,7 +82,8 @@ def test_weights_form_a_distribution_over_the_visible_keys(B, G, Hkv, Nq, Nk, d,
                     assert np.all(oc[b, i, h] == 0.0)
                     continue
                 m = s[i, cols].max()
-                assert m - 1e-12 <= lse[b, h, i] <= m + math.log(cols.size) + 1e-12
+                tol = 1e-12 * max(1.0, abs(m))  # the two sides sum the dot products in different orders
+                assert m - tol <= lse[b, h, i] <= m + math.log(cols.size) + tol
                 lo = vd[b, cols, g].min(axis=0)
                 hi = vd[b, cols, g].max(axis=0)
                 assert np.all(o[b, i, h] >= lo - 1e-12) and np.all(o[b, i, h] <= hi + 1e-12)
