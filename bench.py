@@ -250,18 +250,13 @@ def whole_job_rate(work_per_rank, ms_per_step, world, scale_unit):
     return world * work_per_rank / (ms_per_step * 1e-3) / scale_unit
 
 
-def run_ours(args, w, rank, world, local_rank):
+def setup_workload(w, dev, rank):
+    """Inputs of workload w drawn on the device (seeded CUDA generator, the
+    recipe of workloads.py), outputs and workspace allocated, and one step of
+    the hot path as a closure.  Returns a dict."""
     import torch
-    from exact_io_aware_14_gb300 import _native, build as native_build, workloads as W
+    from exact_io_aware_14_gb300 import _native, workloads as W
 
-    if rank == 0:
-        native_build.build()
-    if world > 1:
-        torch.distributed.barrier()
-        native_build.build()  # no-op once rank 0 has built it
-    _native.lib()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device=dev).manual_seed(1234 + w.seed + rank)
     dec = isinstance(w, W.Decode)
@@ -272,7 +267,6 @@ def run_ours(args, w, rank, world, local_rank):
             x.mul_(amp)
         return x.to(torch.bfloat16)
 
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     if dec:
         q = randn((w.B, 1, w.Hq, w.d))
         k = randn((w.B, w.max_seqlen, w.Hkv, w.d))
@@ -319,11 +313,13 @@ def run_ours(args, w, rank, world, local_rank):
         q = randn((w.B, w.N, w.Hq, w.d), w.amp)
         k = randn((w.B, w.N, w.Hkv, w.d), w.amp)
         v = randn((w.B, w.N, w.Hkv, w.d), w.amp)
+        seqlens = None
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
         work = w.flops()
         unit, scale_unit = "TFLOP/s", 1e12
         launches_per_step = 1
+        dev_inputs = [q, k, v]
 
         if w.window is None:
             def step():
@@ -335,23 +331,35 @@ def run_ours(args, w, rank, world, local_rank):
                 rc = _native.attn_fwd_window(q, k, v, o, lse, w.causal, w.window, w.scale, stream)
                 if rc != 0:
                     raise RuntimeError("attn_fwd_window: %s" % _native.status_string(rc))
+    return {"step": step, "dev_inputs": dev_inputs, "oracle_inputs": (q, k, v), "outputs": (o, lse),
+            "work": work, "unit": unit,
+            "scale_unit": scale_unit, "launches_per_step": launches_per_step, "dec": dec, "seqlens": seqlens,
+            "stream": stream}
 
-    for _ in range(args.warmup):
+
+def time_steps(st, steps, warmup, flush, local_rank, world):
+    """W untimed warm-up steps, then K steps each timed with CUDA events on the
+    launching stream, L2 flushed before every step, clocks sampled meanwhile.
+    Returns (per-step ms list, clock summary, wall seconds)."""
+    import torch
+    from exact_io_aware_14_gb300 import _native
+
+    step, stream = st["step"], st["stream"]
+    for _ in range(warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     if _native.attn_get_device_status(stream) != 0:
         raise RuntimeError("device status error after warm-up")
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     sampler = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     with sampler:
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()
             starts[i].record(stream)
             step()
@@ -362,21 +370,78 @@ def run_ours(args, w, rank, world, local_rank):
         torch.distributed.barrier()
     if _native.attn_get_device_status(stream) != 0:
         raise RuntimeError("device status error in the timed region")
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], sampler.summary(), wall1 - wall0
+
+
+def roofline_of(w, st, kernel_rate, peaks, peak_src):
+    if st["dec"]:
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": kernel_rate, "peak": peak, "unit": "GB/s",
+                "frac": kernel_rate / peak, "traffic": profiled_traffic(w.name),
+                "peak_source": "%s hbm_gbs (copy)" % peak_src,
+                "kernel": "decode split + combine (one step, both launches)",
+                "algorithmic_bytes_per_step": st["work"]}
+    peak = float(peaks["bf16_tflops"])
+    return {"bound": "tensor", "achieved": kernel_rate, "peak": peak, "unit": "TFLOP/s",
+            "frac": kernel_rate / peak, "traffic": profiled_traffic(w.name),
+            "peak_source": "%s bf16_tflops (burst cuBLAS)" % peak_src,
+            "kernel": "prefill_fwd_kernel<%d>" % w.d, "algorithmic_flops_per_launch": st["work"]}
+
+
+def read_rate_gbs(dev, nbytes=4 << 30, reps=5):
+    """HBM read rate of a plain device reduction (torch sum over nbytes of
+    fp32, best of reps, CUDA events): a read-only counterpart of the copy
+    rate, for memory-bound kernels that read far more than they write."""
+    import torch
+    buf = torch.zeros(nbytes // 4, dtype=torch.float32, device=dev)
+    buf.sum()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        buf.sum()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    del buf
+    return nbytes / (best * 1e-3) / 1e9
+
+
+EXTRA_WORKLOADS = ("train", "gqa", "long", "window", "decode", "decode_paged")
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    from exact_io_aware_14_gb300 import _native, build as native_build
+
+    if rank == 0:
+        native_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+        native_build.build()  # no-op once rank 0 has built it
+    _native.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks, peak_src = load_peaks()
+
+    st = setup_workload(w, dev, rank)
+    step, work, unit, scale_unit, dec = st["step"], st["work"], st["unit"], st["scale_unit"], st["dec"]
+    stream = st["stream"]
+    launches_per_step = st["launches_per_step"]
+    step_ms, clocks, timed_wall = time_steps(st, args.steps, args.warmup, flush, local_rank, world)
     total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(work, ms_per_step, world, scale_unit)
     kernel_rate = work / (statistics.mean(step_ms) * 1e-3) / scale_unit
 
     # ---- e2e through host buffers (pinned), copies inside the timed region
-    if dec:
-        h_in = [x.cpu().pin_memory() for x in dev_inputs]
-        d_in = dev_inputs
-        h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (o, lse)]
-    else:
-        h_in = [x.cpu().pin_memory() for x in (q, k, v)]
-        d_in = [q, k, v]
-        h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (o, lse)]
+    o, lse = st["outputs"]
+    d_in = st["dev_inputs"]
+    h_in = [x.cpu().pin_memory() for x in d_in]
+    h_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (o, lse)]
     h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = sum(x.numel() * x.element_size() for x in h_out)
     e2e_steps = max(3, min(args.steps, 20))
@@ -399,41 +464,61 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps, world)
     e2e_value = whole_job_rate(work, e2e_ms, world, scale_unit)
+    del h_in, h_out
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qc, kc, vc = (x.cpu() for x in st["oracle_inputs"])  # the paged workload: its contiguous cache
+        sl = st["seqlens"].cpu().numpy() if dec else None
+        val, dt, desc, thr = oracle_sample_rate(w, qc, kc, vc, sl, args.cpu_seconds, seed=w.seed)
+        cpu = {"value": val, "unit": unit, "cores": thr, "kind": "oracle", "sample": desc}
+        del qc, kc, vc
+    del st, d_in, o, lse
+
+    # ---- every other workload, timed the same way in this process
+    extra = {}
+    if not args.no_workloads:
+        read_gbs = read_rate_gbs(dev) if rank == 0 else None
+        for name in EXTRA_WORKLOADS:
+            w2 = get_workload(name)
+            if w2.name == w.name:
+                continue
+            st2 = setup_workload(w2, dev, rank)
+            ms2, clocks2, wall2 = time_steps(st2, args.workload_steps, args.warmup, flush, local_rank, world)
+            tot2 = max_over_ranks(sum(ms2), world)
+            mps2 = tot2 / args.workload_steps
+            rate2 = st2["work"] / (statistics.mean(ms2) * 1e-3) / st2["scale_unit"]
+            entry = {"workload": w2.name, "value": whole_job_rate(st2["work"], mps2, world, st2["scale_unit"]),
+                     "unit": st2["unit"], "ms_per_step": mps2, "steps": args.workload_steps,
+                     "warmup": args.warmup, "gpu_launches": st2["launches_per_step"] * args.workload_steps,
+                     "roofline": roofline_of(w2, st2, rate2, peaks, peak_src), "clocks": clocks2,
+                     "timed_wall_s": wall2, "config": config_of(w2, world)}
+            entry["frac"] = entry["roofline"]["frac"]
+            if st2["dec"] and read_gbs:
+                entry["read_gbs"] = read_gbs
+                entry["frac_of_read"] = rate2 / read_gbs
+            extra[name] = entry
+            del st2
+            torch.cuda.empty_cache()
+        if rank == 0 and read_gbs:
+            extra["read_probe"] = {"read_gbs": read_gbs,
+                                   "how": "torch sum over 4 GiB of fp32 on this GPU, best of 5, CUDA events"}
 
     if rank != 0:
         return None
-    peaks, peak_src = load_peaks()
-    if dec:
-        peak = float(peaks["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": kernel_rate, "peak": peak, "unit": "GB/s",
-                "frac": kernel_rate / peak, "traffic": profiled_traffic(w.name),
-                "peak_source": "%s hbm_gbs (copy)" % peak_src,
-                "kernel": "decode split + combine (one step, both launches)",
-                "algorithmic_bytes_per_step": work}
-    else:
-        peak = float(peaks["bf16_tflops"])
-        roof = {"bound": "tensor", "achieved": kernel_rate, "peak": peak, "unit": "TFLOP/s",
-                "frac": kernel_rate / peak, "traffic": profiled_traffic(w.name),
-                "peak_source": "%s bf16_tflops (burst cuBLAS)" % peak_src,
-                "kernel": "prefill_fwd_kernel<%d>" % w.d, "algorithmic_flops_per_launch": work}
-
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
-        sl = seqlens.cpu().numpy() if dec else None
-        val, dt, desc, thr = oracle_sample_rate(w, qc, kc, vc, sl, args.cpu_seconds, seed=w.seed)
-        cpu = {"value": val, "unit": unit, "cores": thr, "kind": "oracle", "sample": desc}
-
     return {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) fp32 draws rounded to bf16, generated on the device",
-        "config": config_of(w, world), "roofline": roof, "cpu_baseline": cpu,
+        "config": config_of(w, world), "roofline": roofline_of(w, {"dec": dec, "work": work}, kernel_rate, peaks,
+                                                               peak_src),
+        "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": sampler.summary(),
-        "timed_wall_s": wall1 - wall0,
+        "clocks": clocks,
+        "timed_wall_s": timed_wall,
+        "workloads": extra,
     }
 
 
@@ -482,6 +567,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--reference-seconds", type=float, default=90.0, help="whole reference-arm budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="time only the selected workload")
+    ap.add_argument("--workload-steps", type=int, default=20, help="timed steps of each other workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -160,15 +160,11 @@ size_t attn_splitkv_workspace_size(int B, int Hq, int max_seqlen, int d, int chu
 
 }  // extern "C"
 
-namespace {
+namespace attn {
 
-// Shared by the contiguous and the paged split-KV calls.  Paged: block_table
-// non-null, k/v are page pools [num_pages, page_size, Hkv, d] and the
-// logical cache capacity is max_blocks * page_size.
-attn_status splitkv(const void* q, const void* k, const void* v, const int* seqlens, int max_seqlen,
-                    const int* block_table, int max_blocks, int page_size, int num_pages, void* o, float* lse,
-                    int B, int Hq, int Hkv, int d, float scale, int chunk, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+attn_status check_splitkv_args(const void* q, const void* k, const void* v, const int* seqlens, int max_seqlen,
+                               const int* block_table, int page_size, const void* o, const float* lse, int B, int Hq,
+                               int Hkv, int d, float scale, int chunk) {
   if (B < 1 || Hq < 1 || Hkv < 1 || (Hq % Hkv) != 0 || max_seqlen < 1) return ATTN_ERR_INVALID_ARG;
   if (chunk < 64 || (chunk % 64) != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -186,10 +182,29 @@ attn_status splitkv(const void* q, const void* k, const void* v, const int* seql
     // the pages of one split must fit the kernel's list of them
     if (chunk / page_size + 2 > 128) return ATTN_ERR_UNSUPPORTED;
   }
+  return ATTN_OK;
+}
+
+}  // namespace attn
+
+namespace {
+
+// Shared by the contiguous and the paged split-KV calls.  Paged: block_table
+// non-null, k/v are page pools [num_pages, page_size, Hkv, d] and the
+// logical cache capacity is max_blocks * page_size.
+attn_status splitkv(const void* q, const void* k, const void* v, const int* seqlens, int max_seqlen,
+                    const int* block_table, int max_blocks, int page_size, int num_pages, void* o, float* lse,
+                    int B, int Hq, int Hkv, int d, float scale, int chunk, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  const attn_status st =
+      attn::check_splitkv_args(q, k, v, seqlens, max_seqlen, block_table, page_size, o, lse, B, Hq, Hkv, d, scale,
+                               chunk);
+  if (st != ATTN_OK) return st;
   const size_t need = attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
 
   attn::DecodeParams p;
+
   std::memset(&p, 0, sizeof p);
   const bool ok_maps = block_table ? (make_map(&p.tm_k, k, num_pages, page_size, Hkv, d, 64) &&
                                       make_map(&p.tm_v, v, num_pages, page_size, Hkv, d, 64))

@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/attn.h"
+
 namespace attn {
 
 // Device status codes.  Kernels never trap: a wait that runs out of time
@@ -39,6 +41,13 @@ struct DecodeParams {
   float scale_log2;
 };
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// Host checks of the split-KV decode arguments other than the workspace, in
+// the order the entry points report them (no CUDA call).  block_table is
+// null for a contiguous cache.
+attn_status check_splitkv_args(const void* q, const void* k, const void* v, const int* seqlens, int max_seqlen,
+                               const int* block_table, int page_size, const void* o, const float* lse, int B, int Hq,
+                               int Hkv, int d, float scale, int chunk);
 
 // Reads and clears the device status word of each kernel unit (stream-ordered,
 // then synchronises the stream).  Returns the first non-zero word, or 0.

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/attn.h"
+#include "launch.h"
 
 namespace {
 
@@ -21,7 +22,9 @@ std::mutex g_mutex;
 void* g_addr[kMaxDevices];  // device address of the scratch, per device, once looked up
 
 // Device address of the scratch on the current device (looked up once per
-// device, with that device current).  NULL if the lookup fails.
+// device, with that device current, and kept for the life of the process:
+// a device reset after that first lookup is not supported).  NULL if the
+// lookup fails.
 void* scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -39,6 +42,11 @@ void* scratch_on_current_device() {
 extern "C" attn_status attn_fwd_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                                 const int* seqlens, int max_seqlen, void* o, float* lse, int B,
                                                 int Hq, int Hkv, int d, float scale, int chunk, void* stream) {
+  // every other argument is checked first, with the codes attn_fwd_splitkv
+  // gives them; nothing here touches the GPU before the size check passes
+  const attn_status st = attn::check_splitkv_args(q, k_cache, v_cache, seqlens, max_seqlen, nullptr, 0, o, lse, B,
+                                                  Hq, Hkv, d, scale, chunk);
+  if (st != ATTN_OK) return st;
   const size_t need = attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk);
   if (need > static_cast<size_t>(ATTN_SPLITKV_NOALLOC_MAX_BYTES)) return ATTN_ERR_WORKSPACE;
   void* scratch = scratch_on_current_device();

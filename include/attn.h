@@ -36,6 +36,8 @@
  * this interface.  Problems only the device can see (a pipeline wait that
  * ran out of time, a cache length outside [0, max_seqlen]) are recorded in
  * a library-wide device status word that attn_get_device_status reports.
+ * When it reports ATTN_ERR_TIMEOUT, the o and lse of the calls made since
+ * the previous status read are undefined (they may hold finite values).
  */
 #ifndef ATTN_SM103_H
 #define ATTN_SM103_H
@@ -204,13 +206,22 @@ ATTN_API attn_status attn_fwd_splitkv_paged(const void* q, const void* k_pages, 
  * ATTN_SPLITKV_NOALLOC_MAX_BYTES (8 MiB) in size, which every GPU that loads
  * the library holds until the process exits.  That covers, for example,
  * B=16, Hq=32, d=128, max_seqlen=16384, chunk=1024 (about 4.2 MB).
- *   - Returns ATTN_ERR_WORKSPACE, launching nothing, when
+ *   - Arguments are checked as attn_fwd_splitkv checks them, with the same
+ *     codes, before the size check; then it returns ATTN_ERR_WORKSPACE,
+ *     launching nothing and making no CUDA call, when
  *     attn_splitkv_workspace_size(B, Hq, max_seqlen, d, chunk) exceeds the
- *     scratch size; other argument errors are those of attn_fwd_splitkv.
+ *     scratch size.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
  *   - The first call on a device (with that device current) looks up the
- *     scratch's device address once; make that first call before any stream
- *     capture.  Returns ATTN_ERR_LAUNCH if the lookup fails.
+ *     scratch's device address once and keeps it until the process exits;
+ *     make that first call before any stream capture.  A device reset
+ *     (cudaDeviceReset) after that first call is not supported: the kept
+ *     address would no longer be valid.  Returns ATTN_ERR_LAUNCH if the
+ *     lookup fails.
+ *   - If a split's pipeline wait times out, the combine still reads that
+ *     split's scratch rows, which then hold an earlier call's values: o and
+ *     lse are undefined whenever attn_get_device_status reports
+ *     ATTN_ERR_TIMEOUT.
  *   - Every call on a device shares the one scratch array, which keeps the
  *     last call's contents (nothing needs clearing: each call writes every
  *     partial it reads).  Calls whose kernels may overlap on the GPU (on

@@ -156,3 +156,30 @@ def test_window_argument_checks(L):
     assert _win(L, Nq=0, wl=-7, wr=1 << 30) == 0
     assert _win(L, Nq=(1 << 31) - 200, Nk=100) == 2   # Nq + Nk must leave room below 2^31
     assert _kvc(L, Nq=0, wl=5, wr=-3) == 0
+
+
+def _noalloc(L, **kw):
+    a = dict(q=16, k=16, v=16, s=16, S=2048, o=16, lse=16, B=2, Hq=8, Hkv=2, d=128, scale=0.1, chunk=1024)
+    a.update(kw)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.attn_fwd_splitkv_noalloc(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["s"]), a["S"], vp(a["o"]),
+                                      vp(a["lse"]), a["B"], a["Hq"], a["Hkv"], a["d"], ctypes.c_float(a["scale"]),
+                                      a["chunk"], None)
+
+
+def test_noalloc_refuses_sizes_beyond_its_scratch(L):
+    """The no-allocation decode checks its arguments with attn_fwd_splitkv's
+    codes first, then refuses a problem whose partials exceed its fixed
+    8 MiB scratch; every case here fails before any CUDA call (the pointers
+    are never dereferenced)."""
+    scratch_max = 8 << 20
+    # 64 sequences x 32 heads x 32 splits x (128 + 1) floats: about 33 MB
+    assert L.attn_splitkv_workspace_size(64, 32, 32768, 128, 1024) > scratch_max
+    assert _noalloc(L, B=64, Hq=32, Hkv=8, S=32768) == 7          # ATTN_ERR_WORKSPACE
+    # the other argument errors keep their own codes, also at sizes past the scratch
+    assert _noalloc(L, B=64, Hq=32, Hkv=8, S=32768, d=256) == 2   # unsupported head dim
+    assert _noalloc(L, B=64, Hq=32, Hkv=6, S=32768) == 1          # heads do not divide
+    assert _noalloc(L, B=64, Hq=32, Hkv=8, S=32768, chunk=1000) == 1
+    assert _noalloc(L, B=64, Hq=32, Hkv=8, S=32768, k=24) == 3    # misaligned
+    assert _noalloc(L, B=64, Hq=32, Hkv=8, S=32768, s=0) == 1     # no cache lengths
+    assert _noalloc(L, scale=float("nan")) == 1
