@@ -111,6 +111,23 @@ def test_large_scores_and_constant_rows():
         _full_check(q, k, v, causal, 1 / math.sqrt(d), "large causal=%d" % causal)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_rising_scores_move_the_reference(causal, sign):
+    """Scores that climb by about 17 (natural-log units) every 64 keys: the
+    exponent reference a row set on its first tile must move in both halves
+    of later tiles, including half 1 after half 0's P has gone to the tensor
+    core (the O accumulator is then rescaled in place).  Without the moves
+    the exponentials would overflow fp32 long before the last key; a negative
+    scale runs the same path on -s."""
+    B, H, N, d = 1, 2, 640, 128
+    q, k, v = workloads.prefill_inputs(B, H, H, N, N, d, seed=13)
+    q = torch.ones_like(q)
+    ramp = torch.arange(N, dtype=torch.float32) * (0.26 / math.sqrt(d))
+    k = (sign * ramp[None, :, None, None] * torch.ones((B, 1, H, d))).to(torch.bfloat16)
+    _full_check(q, k, v, causal, sign / math.sqrt(d), "rising scores causal=%d sign %+d" % (causal, sign))
+
+
 def test_repeat_runs_are_bitwise_identical():
     q, k, v = workloads.prefill_inputs(2, 4, 2, 700, 700, 128, seed=9)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
