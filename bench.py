@@ -250,7 +250,7 @@ def whole_job_rate(work_per_rank, ms_per_step, world, scale_unit):
     return world * work_per_rank / (ms_per_step * 1e-3) / scale_unit
 
 
-def setup_workload(w, dev, rank):
+def setup_workload(w, dev, rank, library=None):
     """Inputs of workload w drawn on the device (seeded CUDA generator, the
     recipe of workloads.py), outputs and workspace allocated, and one step of
     the hot path as a closure.  Returns a dict."""
@@ -323,7 +323,7 @@ def setup_workload(w, dev, rank):
 
         if w.window is None:
             def step():
-                rc = _native.attn_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+                rc = _native.attn_fwd(q, k, v, o, lse, w.causal, w.scale, stream, library)
                 if rc != 0:
                     raise RuntimeError("attn_fwd: %s" % _native.status_string(rc))
         else:
@@ -389,19 +389,24 @@ def roofline_of(w, st, kernel_rate, peaks, peak_src):
 
 
 def read_rate_gbs(dev, nbytes=4 << 30, reps=5):
-    """HBM read rate of a plain device reduction (torch sum over nbytes of
-    fp32, best of reps, CUDA events): a read-only counterpart of the copy
-    rate, for memory-bound kernels that read far more than they write."""
+    """HBM read rate of a plain streaming read (the library's read probe: 16-byte
+    loads over nbytes, several in flight per thread), best of reps, CUDA events
+    on the launching stream: the read-only counterpart of the copy rate, for
+    memory-bound kernels that read far more than they write."""
     import torch
-    buf = torch.zeros(nbytes // 4, dtype=torch.float32, device=dev)
-    buf.sum()
+    from exact_io_aware_14_gb300 import _native
+    buf = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+    if _native.attn_probe_read_bandwidth(buf, sink, stream) != 0:
+        raise RuntimeError("read probe failed to launch")
     torch.cuda.synchronize()
     best = None
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        buf.sum()
-        b.record()
+        a.record(stream)
+        _native.attn_probe_read_bandwidth(buf, sink, stream)
+        b.record(stream)
         torch.cuda.synchronize()
         ms = a.elapsed_time(b)
         best = ms if best is None else min(best, ms)
@@ -414,10 +419,12 @@ EXTRA_WORKLOADS = ("train", "gqa", "long", "window", "decode", "decode_paged")
 
 def run_ours(args, w, rank, world, local_rank):
     import torch
-    from exact_io_aware_14_gb300 import _native, build as native_build
+    from exact_io_aware_14_gb300 import _native, build as native_build, workloads as W
 
     if rank == 0:
         native_build.build()
+        if args.exp2_poly:
+            native_build.build_variant("exp2poly%d" % args.exp2_poly)
     if world > 1:
         torch.distributed.barrier()
         native_build.build()  # no-op once rank 0 has built it
@@ -427,7 +434,12 @@ def run_ours(args, w, rank, world, local_rank):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     peaks, peak_src = load_peaks()
 
-    st = setup_workload(w, dev, rank)
+    library = None
+    if args.exp2_poly:
+        if isinstance(w, W.Decode) or w.window is not None:
+            raise SystemExit("--exp2-poly applies to the attn_fwd workloads")
+        library = _native.variant_lib("exp2poly%d" % args.exp2_poly)
+    st = setup_workload(w, dev, rank, library)
     step, work, unit, scale_unit, dec = st["step"], st["work"], st["unit"], st["scale_unit"], st["dec"]
     stream = st["stream"]
     launches_per_step = st["launches_per_step"]
@@ -502,7 +514,8 @@ def run_ours(args, w, rank, world, local_rank):
             torch.cuda.empty_cache()
         if rank == 0 and read_gbs:
             extra["read_probe"] = {"read_gbs": read_gbs,
-                                   "how": "torch sum over 4 GiB of fp32 on this GPU, best of 5, CUDA events"}
+                                   "how": "attn_probe_read_bandwidth: one streaming read of 4 GiB with 16-byte loads, "
+                                          "best of 5, CUDA events"}
 
     if rank != 0:
         return None
@@ -511,7 +524,10 @@ def run_ours(args, w, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) fp32 draws rounded to bf16, generated on the device",
-        "config": config_of(w, world), "roofline": roofline_of(w, {"dec": dec, "work": work}, kernel_rate, peaks,
+        "config": dict(config_of(w, world), **({"exp2": "software exp2 for every %d-th pair of a row's exponentials "
+                                                        "(build variant exp2poly%d)" % (args.exp2_poly, args.exp2_poly)}
+                                                       if args.exp2_poly else {})),
+        "roofline": roofline_of(w, {"dec": dec, "work": work}, kernel_rate, peaks,
                                                                peak_src),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -569,10 +585,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="time only the selected workload")
     ap.add_argument("--workload-steps", type=int, default=20, help="timed steps of each other workload")
+    ap.add_argument("--exp2-poly", type=int, default=0, choices=[0, 2, 4, 8, 16],
+                    help="time the build variant whose softmax computes every K-th pair of exponentials in "
+                         "software (attn_fwd workloads; implies --no-workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = get_workload(args.workload)
+    if args.exp2_poly:
+        args.no_workloads = True
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -43,30 +43,51 @@ def lib():
     if _lib is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError("CUDA attention library not built (%s); run __graft_entry__.build()" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
-        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-        L.attn_fwd.restype = i
-        L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
-        L.attn_fwd_window.restype = i
-        L.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
-        L.attn_fwd_kvcache.restype = i
-        L.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, i, i, f, vp]
-        L.attn_splitkv_workspace_size.restype = sz
-        L.attn_splitkv_workspace_size.argtypes = [i, i, i, i, i]
-        L.attn_fwd_splitkv.restype = i
-        L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp, sz, vp]
-        L.attn_fwd_splitkv_paged.restype = i
-        L.attn_fwd_splitkv_paged.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
-        L.attn_fwd_splitkv_noalloc.restype = i
-        L.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp]
-        L.attn_get_device_status.restype = i
-        L.attn_get_device_status.argtypes = [vp]
-        L.attn_selftest_wait_timeout.restype = i
-        L.attn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
-        L.attn_status_string.restype = ctypes.c_char_p
-        L.attn_status_string.argtypes = [i]
-        _lib = L
+        _lib = _open(LIB_PATH)
     return _lib
+
+
+_variants = {}
+
+
+def variant_lib(name):
+    """A build variant of the library (same interface; see build.VARIANTS),
+    built on first use.  Pass it as ``library=`` to the calls below."""
+    if name not in _variants:
+        from . import build as _build
+        _variants[name] = _open(_build.build_variant(name))
+    return _variants[name]
+
+
+def _open(path):
+    """Loads one build of the library and declares its C signatures."""
+    L = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd.restype = i
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.attn_fwd_window.restype = i
+    L.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, vp]
+    L.attn_fwd_kvcache.restype = i
+    L.attn_fwd_kvcache.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+    L.attn_splitkv_workspace_size.restype = sz
+    L.attn_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    L.attn_fwd_splitkv.restype = i
+    L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    L.attn_fwd_splitkv_paged.restype = i
+    L.attn_fwd_splitkv_paged.argtypes = [vp, vp, vp, vp, i, i, i, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    L.attn_fwd_splitkv_noalloc.restype = i
+    L.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, f, i, vp]
+    L.attn_get_device_status.restype = i
+    L.attn_get_device_status.argtypes = [vp]
+    L.attn_selftest_wait_timeout.restype = i
+    L.attn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_status_string.argtypes = [i]
+    L.attn_selftest_exp2_poly.restype = i
+    L.attn_selftest_exp2_poly.argtypes = [vp, vp, ctypes.c_longlong, vp]
+    L.attn_probe_read_bandwidth.restype = i
+    L.attn_probe_read_bandwidth.argtypes = [vp, sz, vp, vp]
+    return L
 
 
 def status_string(code: int) -> str:
@@ -110,11 +131,12 @@ def _window(window):
     return wl, wr
 
 
-def attn_fwd(q, k, v, o, lse, causal, scale, stream=None):
-    """Same contract as the C call: writes o [B,Nq,Hq,d] and lse [B,Hq,Nq]. Returns the status."""
+def attn_fwd(q, k, v, o, lse, causal, scale, stream=None, library=None):
+    """Same contract as the C call: writes o [B,Nq,Hq,d] and lse [B,Hq,Nq]. Returns the status.
+    library: a build variant from variant_lib(), else the default build."""
     B, Hq, Hkv, Nq, Nk, d = _check_prefill(q, k, v, o, lse)
-    return lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                          int(causal), float(scale), _stream_handle(stream))
+    return (library or lib()).attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                       int(causal), float(scale), _stream_handle(stream))
 
 
 def attn_fwd_window(q, k, v, o, lse, causal, window, scale, stream=None):
@@ -223,18 +245,37 @@ def attn_get_device_status(stream=None):
     return lib().attn_get_device_status(_stream_handle(stream))
 
 
+def attn_selftest_exp2_poly(x, y, stream=None):
+    """y = 2^x by the library's software exp2 (float32 CUDA tensors of one size). Returns the status."""
+    for name, t in (("x", x), ("y", y)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA float32 tensor" % name)
+    if x.numel() != y.numel():
+        raise ValueError("x and y differ in size")
+    return lib().attn_selftest_exp2_poly(_ptr(x), _ptr(y), x.numel(), _stream_handle(stream))
+
+
+def attn_probe_read_bandwidth(buf, sink, stream=None):
+    """One streaming read of the CUDA tensor buf (its bytes; see the C call);
+    sink: a CUDA int64 tensor of one element.  Returns the status."""
+    if not buf.is_cuda or not buf.is_contiguous() or sink.dtype != torch.int64 or not sink.is_cuda:
+        raise ValueError("buf must be a contiguous CUDA tensor and sink a CUDA int64 tensor")
+    return lib().attn_probe_read_bandwidth(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                           _stream_handle(stream))
+
+
 def attn_selftest_wait_timeout(limit_ns, stream=None):
     """Launches the bounded-wait self-test kernel; its timeout shows in attn_get_device_status."""
     return lib().attn_selftest_wait_timeout(int(limit_ns), _stream_handle(stream))
 
 
 # --------------------------------------------------------------------------- convenience wrappers
-def forward(q, k, v, causal, scale, stream=None):
+def forward(q, k, v, causal, scale, stream=None, library=None):
     """Allocates O and LSE with torch on q's device and runs attn_fwd. Returns (o, lse)."""
     B, Nq, Hq, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
-    rc = attn_fwd(q, k, v, o, lse, causal, scale, stream)
+    rc = attn_fwd(q, k, v, o, lse, causal, scale, stream, library)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return o, lse

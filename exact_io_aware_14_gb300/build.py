@@ -1,4 +1,5 @@
-"""Builds the CUDA library in-tree: exact_io_aware_14_gb300/_build/libattn_sm103.so.
+"""Builds the CUDA library in-tree: exact_io_aware_14_gb300/_build/libattn_sm103.so
+(and, on request, build variants under _build/<variant>/).
 
 Each .cu file is compiled by its own nvcc process (in parallel) for sm_103a
 only, then linked into one shared object with the CUDA runtime linked
@@ -33,20 +34,44 @@ def _deps():
                                + glob.glob(os.path.join(ROOT, "include", "*.h"))) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# Build variants: the same sources with preprocessor switches, each in its own
+# directory.  "exp2poly<K>": the prefill softmax computes every K-th pair of
+# exponentials with the software exp2 (csrc/exp2_poly.cuh) instead of MUFU.
+VARIANTS = {"exp2poly%d" % k: ["-DATTN_EXP2_POLY=%d" % k] for k in (2, 4, 8, 16)}
+
+
+def variant_lib_path(name: str) -> str:
+    return os.path.join(OUT_DIR, name, "libattn_sm103.so")
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
+
+
+def build_variant(name: str, force: bool = False, verbose: bool = False) -> str:
+    """Builds the library with the switches of VARIANTS[name] into
+    _build/<name>/libattn_sm103.so (same exported interface)."""
+    defines = VARIANTS[name]
+    lib = variant_lib_path(name)
+    if not force and up_to_date(lib):
+        return lib
+    return _build(os.path.dirname(lib), lib, defines, verbose, False)
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     if not force and up_to_date():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    return _build(OUT_DIR, LIB, [], verbose, ptxas_info)
+
+
+def _build(out_dir, lib, defines, verbose, ptxas_info):
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
-    objs = [os.path.join(OUT_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    objs = [os.path.join(out_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + list(defines)
 
     def compile_one(so):
         s, o = so
@@ -61,15 +86,20 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             sys.stderr.write(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed on %s" % os.path.basename(s))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [NVCC] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc link failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv))
+    names = [a for a in sys.argv[1:] if not a.startswith("--")]
+    if names:
+        for n in names:
+            print(build_variant(n, force="--force" in sys.argv, verbose=True))
+    else:
+        print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv))

@@ -264,6 +264,27 @@ attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream
              : ATTN_ERR_LAUNCH;
 }
 
+attn_status attn_selftest_exp2_poly(const float* x, float* y, long long n, void* stream) {
+  if (n < 0) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  if (!x || !y) return ATTN_ERR_INVALID_ARG;
+  if (n > (1LL << 38)) return ATTN_ERR_UNSUPPORTED;  // grid of 256-thread blocks, one pair per thread
+  if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u)) return ATTN_ERR_MISALIGNED;
+  return attn::launch_selftest_exp2_poly(x, y, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_LAUNCH;
+}
+
+attn_status attn_probe_read_bandwidth(const void* buf, size_t bytes, unsigned long long* sink, void* stream) {
+  if (bytes == 0) return ATTN_OK;
+  if (!buf || !sink) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(buf) || (bytes & 15u) || (reinterpret_cast<uintptr_t>(sink) & 7u)) return ATTN_ERR_MISALIGNED;
+  return attn::launch_read_probe(buf, static_cast<long long>(bytes / 16), sink, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_LAUNCH;
+}
+
 attn_status attn_get_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_LAUNCH;

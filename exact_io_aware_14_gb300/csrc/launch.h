@@ -54,6 +54,8 @@ attn_status check_splitkv_args(const void* q, const void* k, const void* v, cons
 cudaError_t fetch_status_prefill(cudaStream_t stream, uint32_t* out);
 cudaError_t fetch_status_decode(cudaStream_t stream, uint32_t* out);
 cudaError_t launch_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_selftest_exp2_poly(const float* x, float* y, long long n, cudaStream_t stream);
+cudaError_t launch_read_probe(const void* buf, long long n16, unsigned long long* sink, cudaStream_t stream);
 cudaError_t fetch_status_selftest(cudaStream_t stream, uint32_t* out);
 
 }  // namespace attn

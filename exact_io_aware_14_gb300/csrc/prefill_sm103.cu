@@ -36,11 +36,31 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "exp2_poly.cuh"
 #include "launch.h"
 #include "ptx.cuh"
 
+// Build switch: ATTN_EXP2_POLY = K > 0 computes every K-th pair of a row's
+// exponentials with the software exp2 of exp2_poly.cuh (on the FMA and
+// integer pipes) instead of the MUFU unit, as FA4 does on Blackwell; 0 (the
+// default build) uses MUFU for all of them.  K divides 16.
+#ifndef ATTN_EXP2_POLY
+#define ATTN_EXP2_POLY 0
+#endif
+
 namespace attn {
 namespace {
+
+constexpr int kPolyEvery = ATTN_EXP2_POLY;
+static_assert(kPolyEvery == 0 || (kPolyEvery > 0 && 16 % kPolyEvery == 0), "ATTN_EXP2_POLY must divide 16");
+
+// 2^x for the pair of a row's exponentials with pair index i (the index
+// within its 64-column half): MUFU, or the software form for every
+// kPolyEvery-th pair.
+__device__ __forceinline__ float2 exp2_pair(float2 x, int i) {
+  if (kPolyEvery > 0 && (i % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) return exp2_poly2(x);
+  return make_float2(ex2_approx(x.x), ex2_approx(x.y));
+}
 
 __device__ uint32_t g_prefill_status;
 
@@ -147,8 +167,9 @@ __device__ __forceinline__ void half_exp(const uint32_t (&u)[2][32], int h, int 
       v1 = -v1;
     }
     const float2 x = ffma2(make_float2(v0, v1), c2, nmc2);
-    float p0 = ex2_approx(x.x);
-    float p1 = ex2_approx(x.y);
+    const float2 e = exp2_pair(x, i);
+    float p0 = e.x;
+    float p1 = e.y;
     if (kMasked) {  // also right for c == 0, where -inf * 0 would not give 0
       p0 = (64 * h + 2 * i < lim && (!kLo || 64 * h + 2 * i >= lo)) ? p0 : 0.f;
       p1 = (64 * h + 2 * i + 1 < lim && (!kLo || 64 * h + 2 * i + 1 >= lo)) ? p1 : 0.f;
@@ -179,8 +200,9 @@ __device__ __forceinline__ void quarter_exp(const uint32_t (&uq)[32], int q, int
       v1 = -v1;
     }
     const float2 x = ffma2(make_float2(v0, v1), c2, nmc2);
-    float p0 = ex2_approx(x.x);
-    float p1 = ex2_approx(x.y);
+    const float2 e = exp2_pair(x, (q & 1) * 16 + i);
+    float p0 = e.x;
+    float p1 = e.y;
     if (kMasked) {
       p0 = (32 * q + 2 * i < lim && (!kLo || 32 * q + 2 * i >= lo)) ? p0 : 0.f;
       p1 = (32 * q + 2 * i + 1 < lim && (!kLo || 32 * q + 2 * i + 1 >= lo)) ? p1 : 0.f;

@@ -258,6 +258,36 @@ ATTN_API attn_status attn_get_device_status(void* stream);
  */
 ATTN_API attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 
+/*
+ * Self-test of the software exponential: y[i] = 2^x[i] computed the way the
+ * prefill kernel computes a fraction of the softmax's exponentials when the
+ * library is built with ATTN_EXP2_POLY = K > 0 (every K-th pair of a row's
+ * p values), which FA4 does on Blackwell to relieve the MUFU unit
+ * ("FlashAttention: Part 2", sections 1.7 and 1.8).  Cody and Waite's range
+ * reduction x = n + f, |f| <= 1/2, a degree-3 polynomial for 2^f (largest
+ * relative error 1.01e-4 over [-1/2, 1/2]) and n added to the exponent; x is
+ * clamped to [-125, 64] first.  Present in every build (the default build's
+ * prefill uses the MUFU exponential for every p).
+ *   x, y: device float32 arrays of n elements, 4-byte aligned.
+ * Returns ATTN_OK once launched on `stream`; ATTN_ERR_INVALID_ARG for n < 0
+ * or a NULL pointer (n > 0).
+ */
+ATTN_API attn_status attn_selftest_exp2_poly(const float* x, float* y, long long n, void* stream);
+
+/*
+ * Measurement helper: reads `bytes` of device memory at `buf` once, as a
+ * plain stream of 16-byte loads with several in flight per thread over the
+ * whole GPU, and XORs a fold of the data into *sink (device memory, 8-byte
+ * aligned; its value is meaningless, it only keeps the loads).  Timed on a
+ * buffer far larger than L2, it gives the HBM read rate a read-bound kernel
+ * (the split-KV decode) is measured against, next to the copy rate.  The
+ * pages have no counterpart to this call.
+ *   buf: 16-byte aligned, bytes a multiple of 16.
+ * Returns ATTN_OK once launched on `stream`.
+ */
+ATTN_API attn_status attn_probe_read_bandwidth(const void* buf, size_t bytes, unsigned long long* sink,
+                                               void* stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 ATTN_API const char* attn_status_string(attn_status s);
 

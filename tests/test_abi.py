@@ -183,3 +183,18 @@ def test_noalloc_refuses_sizes_beyond_its_scratch(L):
     assert _noalloc(L, B=64, Hq=32, Hkv=8, S=32768, k=24) == 3    # misaligned
     assert _noalloc(L, B=64, Hq=32, Hkv=8, S=32768, s=0) == 1     # no cache lengths
     assert _noalloc(L, scale=float("nan")) == 1
+
+
+def test_selftest_and_probe_argument_checks(L):
+    """Host checks of the software-exp2 self-test and the read probe (no CUDA
+    call is made for any of these)."""
+    vp = ctypes.c_void_p
+    assert L.attn_selftest_exp2_poly(None, None, 0, None) == 0          # nothing to do
+    assert L.attn_selftest_exp2_poly(None, None, -1, None) == 1
+    assert L.attn_selftest_exp2_poly(vp(16), None, 8, None) == 1
+    assert L.attn_selftest_exp2_poly(vp(18), vp(16), 8, None) == 3      # not 4-byte aligned
+    assert L.attn_probe_read_bandwidth(None, 0, None, None) == 0
+    assert L.attn_probe_read_bandwidth(None, 64, vp(16), None) == 1
+    assert L.attn_probe_read_bandwidth(vp(24), 64, vp(16), None) == 3   # buffer not 16-byte aligned
+    assert L.attn_probe_read_bandwidth(vp(32), 40, vp(16), None) == 3   # size not a multiple of 16
+    assert L.attn_probe_read_bandwidth(vp(32), 64, vp(12), None) == 3   # sink not 8-byte aligned
