@@ -12,6 +12,8 @@ Default workload: the training shape B=4, H=16, N=4096, d=128, causal.
 value: device-resident throughput (inputs already in HBM), CUDA events around
 each step on the launching stream, L2 flushed (256 MB write) before every
 timed step, summed over K steps, max over ranks; whole-job aggregate.
+sustained: the same step back to back for about two seconds (no flush; the
+inputs exceed L2), with its own clock samples.
 e2e: the same metric through the same C-ABI call with host buffers: every
 step copies the inputs from pinned host memory and the outputs back; the
 copies of consecutive steps overlap the compute on their own streams
@@ -498,6 +500,30 @@ def run_ours(args, w, rank, world, local_rank):
     value = whole_job_rate(work, ms_per_step, world, scale_unit)
     kernel_rate = work / (statistics.mean(step_ms) * 1e-3) / scale_unit
 
+    # ---- sustained: the same step back to back for about two seconds, one
+    # event pair around the block, clocks sampled meanwhile (inputs larger
+    # than L2 stand in for the flush)
+    sustained = None
+    if not args.no_sustained and not args.no_workloads:
+        in_bytes = sum(x.numel() * x.element_size() for x in st["dev_inputs"])
+        n_sus = max(10, int(args.sustained_seconds * 1e3 / max(statistics.mean(step_ms), 1e-3)))
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sus_sampler = ClockSampler(local_rank)
+        torch.cuda.synchronize()
+        with sus_sampler:
+            a_ev.record(stream)
+            for _ in range(n_sus):
+                step()
+            b_ev.record(stream)
+            torch.cuda.synchronize()
+        if _native.attn_get_device_status(stream) != 0:
+            raise RuntimeError("device status error in the sustained block")
+        sus_ms = max_over_ranks(a_ev.elapsed_time(b_ev), world) / n_sus
+        sustained = {"value": whole_job_rate(work, sus_ms, world, scale_unit), "unit": unit, "steps": n_sus,
+                     "ms_per_step": sus_ms, "clocks": sus_sampler.summary(),
+                     "l2": "not flushed: inputs of %.0f MB, larger than L2" % (in_bytes / 1e6)
+                     if in_bytes > 129e6 else "not flushed; inputs of %.0f MB fit L2" % (in_bytes / 1e6)}
+
     # ---- e2e through host buffers (pinned), copies inside the timed region
     o, lse = st["outputs"]
     d_in = st["dev_inputs"]
@@ -599,6 +625,7 @@ def run_ours(args, w, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "timed_wall_s": timed_wall,
+        "sustained": sustained,
         "workloads": extra,
     }
 
@@ -648,7 +675,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--reference-seconds", type=float, default=90.0, help="whole reference-arm budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-workloads", action="store_true", help="time only the selected workload")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the K steps of the selected workload (no other workloads, no sustained block)")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the two-second back-to-back block")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0)
     ap.add_argument("--workload-steps", type=int, default=20, help="timed steps of each other workload")
     ap.add_argument("--exp2-poly", type=int, default=0, choices=[0, 2, 4, 8, 16],
                     help="time the build variant whose softmax computes every K-th pair of exponentials in "
