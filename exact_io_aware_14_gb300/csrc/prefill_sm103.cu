@@ -356,7 +356,11 @@ __device__ __forceinline__ float score_tile_onepass(uint32_t tS, int lo, int lim
 // Work unit U -> (batch, KV head, the two query tiles).  Units are numbered
 // (u_rev, head slot, batch) with u_rev slowest, so units whose rows see a
 // right-bounded key range (causal, or a window's right side) come longest
-// first.  Keys of the unit's sequence: nk (Nk, or its cache length when
+// first and every round holds units of about one length, which the zig-zag
+// balances.  kSlotMajor (the instance for no mask, where all units of a slot
+// are equally long) numbers them (head slot, batch, u_rev) with u_rev
+// fastest instead: the CTAs of a round then share a few heads' K and V,
+// which come from L2 after their first read.  Keys of the unit's sequence: nk (Nk, or its cache length when
 // seqlens is given); key j is visible to row i iff j < nk, j <= i + coff and,
 // in the general form, j >= i + lo.  causal 1 aligns top-left (coff = 0), 2
 // bottom-right (coff = nk - Nq); a local window (wl, wr) is aligned
@@ -370,14 +374,20 @@ struct Unit {
   bool rot;  // visit kt0 last (key_tile)
   TileInfo ti[2];
 };
-template <bool kGeneral>
+template <bool kGeneral, bool kSlotMajor = false>
 __device__ __forceinline__ Unit decode_unit(int U, int B, int Hq, int Hkv, int Nq, int Nk, int causal, int wl, int wr,
                                             const int* __restrict__ seqlens, int pair_heads, int units_per_bh) {
   Unit u;
   const int hslots = pair_heads ? Hq / 2 : Hq;
   const int bh_count = B * hslots;
-  const int u_rev = U / bh_count;
-  const int bh = U % bh_count;
+  int u_rev, bh;
+  if (kSlotMajor) {
+    bh = U / units_per_bh;
+    u_rev = U % units_per_bh;
+  } else {
+    u_rev = U / bh_count;
+    bh = U % bh_count;
+  }
   const bool rev = (causal != 0) || (kGeneral && wr >= 0);
   const int unit = rev ? (units_per_bh - 1 - u_rev) : u_rev;
   u.b = bh / hslots;
@@ -461,7 +471,7 @@ __device__ __forceinline__ int unit_of_round(int r, int total_units) {
 // kGeneral: keys per sequence may come from seqlens (attn_fwd_kvcache) and
 // the mask may have a local window; otherwise every sequence has Nk keys,
 // seqlens is not read and the mask is at most causal.
-template <int D, bool kNeg, bool kGeneral>
+template <int D, bool kNeg, bool kGeneral, bool kSlotMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
@@ -540,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit<kGeneral>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads, units_per_bh);
+        const Unit u = decode_unit<kGeneral, kSlotMajor>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads,
+                                                          units_per_bh);
         if (kGeneral && lens && (lens[u.b] < 0 || lens[u.b] > Nk) && u.ti[0].hq == 0) record(11, kDevBadSeqlen);
         for (int t = 0; t < 2; ++t) {
           // Q_t of the previous unit must have been read by its last QK^T
@@ -622,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
         const int U = unit_of_round(rnd, total_units);
         if (U < 0) continue;
-        const Unit u = decode_unit<kGeneral>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads, units_per_bh);
+        const Unit u = decode_unit<kGeneral, kSlotMajor>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads,
+                                                          units_per_bh);
         const int n_kt = u.n_kt;
         for (int t = 0; t < 2 && ok; ++t) {
           ok = wait_one(bar_qfull + t, uc & 1, abort_flag, 3);
@@ -792,7 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rnd = 0; ok && rnd * static_cast<int>(gridDim.x) < total_units; ++rnd) {
       const int U = unit_of_round(rnd, total_units);
       if (U < 0) continue;
-      const Unit u = decode_unit<kGeneral>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads, units_per_bh);
+      const Unit u = decode_unit<kGeneral, kSlotMajor>(U, B, Hq, Hkv, Nq, Nk, causal, wl, wr, lens, pair_heads,
+                                                          units_per_bh);
       const TileInfo me = t ? u.ti[1] : u.ti[0];
       const int grow = me.row0 + r;
       const int my_kt = me.n_kt;
@@ -941,8 +954,10 @@ cudaError_t launch_d(const PrefillParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(total < n_sm ? total : n_sm);  // one persistent CTA per SM
   const bool general = p.seqlens || p.window_left >= 0 || p.window_right >= 0;
-  auto kern = general ? ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, true> : prefill_fwd_kernel<D, false, true>)
-                      : ((p.scale_log2 < 0.f) ? prefill_fwd_kernel<D, true, false> : prefill_fwd_kernel<D, false, false>);
+  const bool neg = p.scale_log2 < 0.f;
+  auto kern = general        ? (neg ? prefill_fwd_kernel<D, true, true, false> : prefill_fwd_kernel<D, false, true, false>)
+              : p.causal == 0 ? (neg ? prefill_fwd_kernel<D, true, false, true> : prefill_fwd_kernel<D, false, false, true>)
+                              : (neg ? prefill_fwd_kernel<D, true, false, false> : prefill_fwd_kernel<D, false, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, L::kAlloc, stream>>>(p.tm_q, p.tm_k, p.tm_v, static_cast<__nv_bfloat16*>(p.o), p.lse, p.B,
