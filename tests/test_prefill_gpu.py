@@ -64,6 +64,8 @@ def test_tiny_workload_full():
     (3, 40, 40, 300, 300, 128, True),
     (3, 40, 40, 300, 300, 64, False),
     (2, 32, 8, 700, 700, 128, True),    # GQA head pairs, 192 units
+    (2, 64, 16, 700, 700, 128, False),  # no mask: units head slot by head slot, GQA pairs, 384 units
+    (5, 24, 24, 520, 520, 64, False),   # no mask, consecutive row tiles, odd tile count, 240 units
     (2, 96, 32, 130, 390, 128, True),   # group size 3: consecutive row tiles
 ])
 def test_small_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
