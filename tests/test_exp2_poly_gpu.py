@@ -99,3 +99,21 @@ def test_training_workload_with_software_exp2_every_row():
     del o, lse
     o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.causal, w.scale)
     compare(o_gpu, lse_gpu, o_ref, lse_ref, w.name + " with the software exp2")
+
+
+def test_read_probe_reads_every_word():
+    """attn_probe_read_bandwidth folds every 16-byte word of the buffer into
+    its sink by XOR: over a buffer whose words XOR to a known value the sink
+    must hold it (no load skipped, none read twice), including a ragged tail
+    that is not a multiple of the grid's stride."""
+    n_words = (64 << 20) // 4 + 12  # 64 MB plus three 16-byte words
+    buf = torch.zeros(n_words, dtype=torch.int32, device="cuda")
+    buf[5] = 0x12345678
+    buf[n_words - 1] = 0x0F0F0F0F      # in the last 16-byte word
+    buf[n_words // 2] = 0x00FF00FF
+    sink = torch.zeros(1, dtype=torch.int64, device="cuda")
+    assert _native.attn_probe_read_bandwidth(buf, sink) == 0
+    torch.cuda.synchronize()
+    expect = 0x12345678 ^ 0x0F0F0F0F ^ 0x00FF00FF
+    assert int(sink.item()) == expect
+    assert _native.attn_get_device_status() == 0
