@@ -40,3 +40,23 @@ def test_bench_line(workload, unit, launches):
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert "sm_max_mhz" in d["clocks"] and "reasons" in d["clocks"]
     assert d["config"]["workload"]
+
+
+def test_bench_line_with_every_workload():
+    """The default run's extra objects on short settings: every other workload
+    timed in the same process with its own roofline and clocks, the decode
+    entries measured against the read probe as well, the sustained block."""
+    d = _bench("--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--workload-steps", "3",
+               "--sustained-seconds", "0.2")
+    wl = d["workloads"]
+    for name in ("train", "gqa", "long", "window", "decode", "decode_paged"):
+        e = wl[name]
+        assert e["value"] > 0 and e["steps"] == 3 and e["roofline"]["peak"] > 0, name
+        assert abs(e["frac"] - e["roofline"]["achieved"] / e["roofline"]["peak"]) < 1e-9, name
+        assert "sm_max_mhz" in e["clocks"], name
+    for name in ("decode", "decode_paged"):
+        assert wl[name]["read_gbs"] > 0 and wl[name]["frac_of_read"] > 0
+    assert wl["read_probe"]["read_gbs"] > 0
+    s = d["sustained"]
+    assert s["value"] > 0 and s["steps"] >= 10 and "sm_mhz" in s["clocks"]
+    assert d["e2e_serial"]["value"] > 0
